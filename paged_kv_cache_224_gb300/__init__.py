@@ -1,0 +1,1 @@
+"""Paged-KV decode attention for GB300 (sm_103a)."""
