@@ -1,0 +1,392 @@
+#!/usr/bin/env python3
+"""Benchmark of one paged-KV decode step on GB300.
+
+A step is one pass of the hot path over one batch: ``pa_reshape_and_cache``
+writes each sequence's new K/V token into its slot, then ``pa_decode``
+attends every sequence over its paged cache (split-K partitions + log-sum-exp
+reduce where a sequence spans several partitions).
+
+Default workload: LLaMA-style GQA decode -- 256 sequences, 32 query heads,
+8 KV heads, head_dim 128, bf16, block_size 16, context lengths U{1..4096},
+blocks scattered over a pool 1.25x the size needed (2.7 GB, far larger than
+L2, so no step re-reads the previous step's data from L2).
+
+Output: one JSON line (rank 0).  ``value`` is achieved HBM GB/s of the whole
+step: algorithmic bytes (valid K/V rows once per kv head + Q + out + tables
++ lengths for the decode, new rows + slots for the cache write) over device
+time.  ``--impl reference`` times the CPU oracle instead, on a bounded sample.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+METRIC = "paged decode attention: achieved HBM GB/s (% of GB300 peak) and tokens/s"
+FALLBACK_HBM_GBS = 6800.0
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    return FALLBACK_HBM_GBS, "fallback"
+
+
+def load_traffic(kernel_key: str):
+    """Per-launch DRAM bytes of the decode kernel from the committed ncu
+    summary, if it was taken on the current kernel source."""
+    path = os.path.join(ROOT, "profiles", "traffic.txt")
+    if not os.path.exists(path):
+        return None
+    import hashlib
+    src = os.path.join(ROOT, "paged_kv_cache_224_gb300", "csrc", "pa_decode.cuh")
+    sha = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+    for line in open(path):
+        parts = line.split()
+        if len(parts) >= 3 and parts[0] == kernel_key and parts[1] == sha:
+            return float(parts[2])
+    return None
+
+
+class ClockSampler:
+    """Samples SM clocks and throttle reasons with nvidia-smi while running."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "50"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        time.sleep(0.15)
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            time.sleep(0.1)
+            self.proc.terminate()
+            try:
+                self.out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                self.out = ""
+        return False
+
+    def summary(self):
+        if self.proc is None:
+            return None
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in (self.out or "").splitlines():
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 8:
+                continue
+            try:
+                sm.append(float(f[0]))
+                mx.append(float(f[1]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[4:8]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "samples": len(sm),
+                "reasons": sorted(reasons)}
+
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def max_over_ranks(x: float, world: int, device) -> float:
+    if world == 1:
+        return x
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def sum_over_ranks(x: float, world: int, device) -> float:
+    if world == 1:
+        return x
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.SUM)
+    return float(t.item())
+
+
+def barrier(world: int):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def make_case(name: str, seed_offset: int):
+    from paged_kv_cache_224_gb300 import workload as wl
+    if name == "llama_gqa":
+        return wl.llama_gqa_case(seed=1002 + seed_offset)
+    if name == "opt13b_mha":
+        return wl.opt13b_case(seed=1001 + seed_offset)
+    if name == "long_context":
+        return wl.long_context_case(seed=1004 + seed_offset)
+    raise SystemExit(f"unknown workload {name}")
+
+
+def cpu_oracle_sample(case, tensors, nseq: int, threads: int):
+    """Time the CPU oracle on the first ``nseq`` sequences of the step.
+    Returns (seconds, algorithmic bytes of the sample)."""
+    import oracle
+    sys.path.insert(0, os.path.join(ROOT, "tests"))
+    from tests.helpers import oracle_inputs
+    oracle.build()
+    seqs = list(range(min(nseq, case.num_seqs)))
+    inp = oracle_inputs(case, tensors, seqs)
+    kc, vc = inp["k_cache"], inp["v_cache"]
+    lens = inp["context_lens"]
+    t0 = time.perf_counter()
+    oracle.reshape_and_cache(inp["new_key"], inp["new_value"], kc, vc, inp["slot_mapping"], case.block_size)
+    oracle.decode(inp["query"], kc, vc, inp["block_tables"], lens, case.scale, case.dtype,
+                  num_threads=threads)
+    dt = time.perf_counter() - t0
+    el = 2
+    kv = int(lens.astype(np.int64).sum()) * 2 * case.num_kv_heads * case.head_dim * el
+    q = len(seqs) * case.num_heads * case.head_dim * el
+    return dt, kv + 2 * q
+
+
+def run_reference(args, world, rank):
+    """The CPU oracle as the reference arm: each step is one oracle decode
+    over a bounded sample of the workload's sequences."""
+    if rank != 0:
+        return
+    case = make_case(args.workload, 0)
+    tensors = case.materialize("cpu")
+    threads = os.cpu_count() or 1
+    nseq = args.ref_seqs
+    for _ in range(args.warmup):
+        cpu_oracle_sample(case, tensors, nseq, threads)
+    total_t, total_b = 0.0, 0
+    for _ in range(args.steps):
+        dt, b = cpu_oracle_sample(case, tensors, nseq, threads)
+        total_t += dt
+        total_b += b
+    gbs = total_b / total_t / 1e9
+    line = {"impl": "reference", "metric": METRIC, "value": round(gbs, 3), "unit": "GB/s",
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(1e3 * total_t / args.steps, 3), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": case.name, "sample_seqs": min(nseq, case.num_seqs)},
+            "cpu_baseline": {"value": round(gbs, 3), "unit": "GB/s", "cores": threads, "kind": "oracle",
+                             "sample": f"first {min(nseq, case.num_seqs)} of {case.num_seqs} sequences "
+                                       f"of {case.name}, cache write + decode, per step"},
+            "e2e": {"value": round(gbs, 3), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=500)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="llama_gqa", choices=["llama_gqa", "opt13b_mha", "long_context"])
+    ap.add_argument("--partition-tokens", type=int, default=0)
+    ap.add_argument("--e2e-steps", type=int, default=50)
+    ap.add_argument("--cpu-seqs", type=int, default=64, help="sequences in the CPU-baseline sample")
+    ap.add_argument("--ref-seqs", type=int, default=2, help="sequences per reference-arm step")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+
+    world, rank, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl" if args.impl == "ours" else "gloo")
+    if args.impl == "reference":
+        run_reference(args, world, rank)
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+        return
+
+    import paged_kv_cache_224_gb300 as pa
+    from paged_kv_cache_224_gb300 import build as pa_build
+    pa_build.build()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    stream = torch.cuda.current_stream(dev)
+
+    case = make_case(args.workload, rank)
+    t = case.materialize(dev)
+    tensors_host_copy_needed = rank == 0 and not args.no_cpu_baseline
+    cpu_sample = None
+    if tensors_host_copy_needed:
+        # the oracle reads the pre-step pool: take its sample before any kernel runs
+        cpu_sample = cpu_oracle_sample(case, t, args.cpu_seqs, os.cpu_count() or 1)
+
+    slots = torch.as_tensor(case.slot_mapping, device=dev)
+    bt = torch.as_tensor(case.block_tables, device=dev)
+    lens = torch.as_tensor(case.context_lens, device=dev)
+    out = torch.empty_like(t["query"])
+    pt = args.partition_tokens
+    ws = pa.decode_workspace(t["query"], case.block_size, case.max_context_len, pt)
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    part = pa.pa_decode_partition_tokens(case.num_seqs, case.num_kv_heads, case.block_size,
+                                         case.max_context_len, pt)
+    max_parts = -(-case.max_context_len // part)
+    launches_per_step = 1 + 1 + (1 if max_parts > 1 else 0)
+
+    def step():
+        pa.pa_reshape_and_cache(t["new_key"], t["new_value"], t["k_cache"], t["v_cache"], slots, d_err=err)
+        pa.pa_decode(out, t["query"], t["k_cache"], t["v_cache"], bt, lens, case.scale,
+                     case.max_context_len, partition_tokens=pt, workspace=ws, d_err=err)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    if int(err.item()) != 0:
+        raise SystemExit(f"device error flags {int(err.item()):#x}")
+
+    # ---- device-timed region: K steps, inputs resident in HBM
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(args.steps)]
+    barrier(world)
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk:
+        start = torch.cuda.Event(enable_timing=True)
+        stop = torch.cuda.Event(enable_timing=True)
+        start.record(stream)
+        for i in range(args.steps):
+            pa.pa_reshape_and_cache(t["new_key"], t["new_value"], t["k_cache"], t["v_cache"], slots, d_err=err)
+            ev[i][0].record(stream)
+            pa.pa_decode(out, t["query"], t["k_cache"], t["v_cache"], bt, lens, case.scale,
+                         case.max_context_len, partition_tokens=pt, workspace=ws, d_err=err)
+            ev[i][1].record(stream)
+        stop.record(stream)
+        torch.cuda.synchronize()
+    barrier(world)
+    elapsed_ms = start.elapsed_time(stop)
+    decode_ms = [a.elapsed_time(b) for a, b in ev]
+    elapsed_ms = max_over_ranks(elapsed_ms, world, dev)
+
+    step_bytes = case.decode_bytes() + case.reshape_bytes()
+    total_bytes = sum_over_ranks(float(step_bytes) * args.steps, world, dev)
+    gbs = total_bytes / (elapsed_ms / 1e3) / 1e9
+    ms_per_step = elapsed_ms / args.steps
+    tokens_per_s = sum_over_ranks(float(case.num_seqs), world, dev) / (ms_per_step / 1e3)
+
+    peak, peak_kind = load_peaks()
+    dec_avg_ms = statistics.mean(decode_ms)
+    dec_achieved = case.decode_bytes() / (dec_avg_ms / 1e3) / 1e9
+    kernel_key = f"decode_{case.name}"
+    traffic = load_traffic(kernel_key)
+
+    # ---- end to end through the C ABI: host buffers in, result out
+    h_q = t["query"].cpu().pin_memory()
+    h_nk = t["new_key"].cpu().pin_memory()
+    h_nv = t["new_value"].cpu().pin_memory()
+    h_slots = slots.cpu().pin_memory()
+    h_bt = bt.cpu().pin_memory()
+    h_lens = lens.cpu().pin_memory()
+    h_out = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    d_q, d_nk, d_nv = torch.empty_like(t["query"]), torch.empty_like(t["new_key"]), torch.empty_like(t["new_value"])
+    d_slots, d_bt, d_lens = torch.empty_like(slots), torch.empty_like(bt), torch.empty_like(lens)
+    h2d = sum(x.numel() * x.element_size() for x in (h_q, h_nk, h_nv, h_slots, h_bt, h_lens))
+    d2h = h_out.numel() * h_out.element_size()
+
+    def e2e_step():
+        for d, h in ((d_q, h_q), (d_nk, h_nk), (d_nv, h_nv), (d_slots, h_slots), (d_bt, h_bt), (d_lens, h_lens)):
+            d.copy_(h, non_blocking=True)
+        pa.pa_reshape_and_cache(d_nk, d_nv, t["k_cache"], t["v_cache"], d_slots, d_err=err)
+        pa.pa_decode(out, d_q, t["k_cache"], t["v_cache"], d_bt, d_lens, case.scale,
+                     case.max_context_len, partition_tokens=pt, workspace=ws, d_err=err)
+        h_out.copy_(out, non_blocking=True)
+
+    for _ in range(3):
+        e2e_step()
+    torch.cuda.synchronize()
+    barrier(world)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.e2e_steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1), world, dev) / args.e2e_steps
+    e2e_bytes = sum_over_ranks(float(step_bytes), world, dev)
+    e2e_gbs = e2e_bytes / (e2e_ms / 1e3) / 1e9
+    if int(err.item()) != 0:
+        raise SystemExit(f"device error flags {int(err.item()):#x}")
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": round(gbs, 2), "unit": "GB/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": case.dtype,
+            "data": "synthetic",
+            "config": {"workload": case.name, "num_seqs": case.num_seqs, "num_heads": case.num_heads,
+                       "num_kv_heads": case.num_kv_heads, "head_dim": case.head_dim,
+                       "block_size": case.block_size, "context_lens": "uniform, see workload",
+                       "max_context_len": case.max_context_len, "partition_tokens": part,
+                       "pool_blocks": case.num_blocks,
+                       "l2": "inputs larger than L2: KV pool %.2f GB, %.2f GB read per step" % (
+                           2 * case.num_blocks * case.num_kv_heads * case.block_size * case.head_dim * 2 / 1e9,
+                           case.kv_bytes() / 1e9),
+                       "step": "pa_reshape_and_cache (1 token/seq) + pa_decode",
+                       "parallelism": f"replicas x{world}, sequences sharded, no collective"},
+            "pct_of_peak": round(100 * gbs / peak, 2),
+            "tokens_per_s": round(tokens_per_s, 1),
+            "context_tokens_per_s": round(float(case.context_lens.sum()) * world / (ms_per_step / 1e3), 1),
+            "roofline": {"bound": "hbm", "achieved": round(dec_achieved, 2), "peak": peak,
+                         "unit": "GB/s", "frac": round(dec_achieved / peak, 4), "traffic": traffic,
+                         "kernel": "pa_decode (decode_kernel + decode_reduce_kernel)",
+                         "bytes_per_launch": case.decode_bytes(), "avg_ms": round(dec_avg_ms, 5),
+                         "peak_kind": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured" else "fallback"},
+            "e2e": {"value": round(e2e_gbs, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d,
+                    "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 5)},
+            "gpu_launches": launches_per_step * args.steps,
+            "clocks": clk.summary(),
+        }
+        if cpu_sample is not None:
+            dt, b = cpu_sample
+            line["cpu_baseline"] = {"value": round(b / dt / 1e9, 4), "unit": "GB/s",
+                                    "cores": os.cpu_count() or 1, "kind": "oracle",
+                                    "sample": f"first {min(args.cpu_seqs, case.num_seqs)} of {case.num_seqs} "
+                                              f"sequences of {case.name}: cache write + decode, fp64"}
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

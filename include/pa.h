@@ -1,0 +1,179 @@
+/*
+ * pa.h -- C ABI of the paged-KV attention library (GB300, sm_103a).
+ *
+ * The operations follow the pages on vLLM's PagedAttention:
+ *   "vLLM PagedAttention chuyen sau: Phan manh bo nho KV Cache, Prefill theo
+ *   khoi & Prefix Caching" (locionic.com) -- sections "Tuong tu phan trang bo
+ *   nho ao" (logical blocks, physical blocks, block table, dynamic growth),
+ *   "Co che PagedAttention" (look up, gather, attend), "Chunked Prefill"
+ *   (mechanism, KV accumulation) and "Co che APC" step 3 (copy-on-write);
+ *   "vLLM" (tellworld.net), section "PagedAttention" (fixed-size blocks
+ *   located through a table; sharing).
+ *
+ * Conventions for every entry point
+ * ---------------------------------
+ * Pointers.  Every data pointer is a DEVICE pointer owned by the caller; the
+ *   library allocates nothing and keeps no pointer after a call returns.
+ *   16-bit tensors must be 16-byte aligned.  The only host arguments are the
+ *   scalars.
+ * Streams.  `stream` is a cudaStream_t passed as void* (NULL = legacy default
+ *   stream).  Every call only enqueues work on it and returns; results are
+ *   ready when the stream is synchronised.
+ * Cache layout.  k_cache and v_cache are each
+ *   [num_blocks][num_kv_heads][block_size][head_dim], row-major, elements of
+ *   `dtype`.  Token slot t of the pool is block t / block_size, offset
+ *   t % block_size.  One (block, kv head) tile is block_size*head_dim
+ *   contiguous elements.
+ * Head grouping.  Query head h reads KV head h / (num_heads / num_kv_heads).
+ * Argument errors (null pointers, bad sizes, unsupported shapes, misaligned
+ *   pointers, a too-small workspace) are found on the host before anything
+ *   is launched: the call returns a negative pa_status and enqueues nothing.
+ * Data errors (a slot or table entry outside the pool, a context length past
+ *   the table, a conflicting copy pair, a pipeline wait that gave up) are
+ *   found on the device: the offending unit is skipped and a PA_DEVERR_* bit
+ *   is OR-ed into *d_err (d_err may be NULL to ignore them).  No kernel traps;
+ *   the context stays usable.  Read *d_err after the stream synchronises.
+ */
+#ifndef PA_H
+#define PA_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define PA_API __attribute__((visibility("default")))
+#else
+#define PA_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum { PA_F16 = 0, PA_BF16 = 1 } pa_dtype;
+
+typedef enum {
+    PA_OK = 0,
+    PA_ERR_INVALID_ARG = -1,   /* null pointer, non-positive size, bad enum */
+    PA_ERR_UNSUPPORTED = -2,   /* a shape this build has no kernel for */
+    PA_ERR_OUT_OF_RANGE = -3,  /* a host scalar outside its allowed range */
+    PA_ERR_CUDA = -4,          /* a CUDA runtime call failed (launch, attribute) */
+    PA_ERR_WORKSPACE = -5,     /* workspace missing or smaller than required */
+    PA_ERR_ALIGNMENT = -6      /* a pointer is not 16-byte aligned */
+} pa_status;
+
+/* Bits OR-ed into *d_err by the kernels. */
+#define PA_DEVERR_SLOT_RANGE 0x1    /* slot_mapping entry >= num_blocks*block_size */
+#define PA_DEVERR_BLOCK_RANGE 0x2   /* block-table entry outside [0, num_blocks) */
+#define PA_DEVERR_CONTEXT_RANGE 0x4 /* context length < 0, > max_context_len or > table */
+#define PA_DEVERR_COPY_PAIR 0x8     /* copy pair out of pool, src==dst, or dst conflict */
+#define PA_DEVERR_TIMEOUT 0x10      /* a bounded pipeline wait gave up */
+
+/* Human-readable name of a pa_status value. */
+PA_API const char *pa_status_string(int status);
+
+/*
+ * pa_reshape_and_cache -- write new tokens' K and V rows into their slots.
+ * (Dynamic growth of a sequence: each new token lands in a slot of one of
+ * its physical blocks; chunked prefill accumulates a chunk's KV the same way.)
+ *
+ *   key, value     [num_tokens][num_kv_heads][head_dim] dtype, contiguous
+ *   k_cache,v_cache pool as above, written in place
+ *   slot_mapping   int64 [num_tokens]; slot < 0 = padding, nothing written;
+ *                  slot >= num_blocks*block_size sets PA_DEVERR_SLOT_RANGE
+ * Requires head_dim % 8 == 0.  num_tokens == 0 is a no-op.  Two tokens with
+ * the same slot race (one of them wins); the caller must not do that.
+ * The copy is bit-exact.
+ */
+PA_API int pa_reshape_and_cache(const void *key, const void *value, void *k_cache, void *v_cache,
+                         const int64_t *slot_mapping, int num_tokens, int num_kv_heads,
+                         int head_dim, int block_size, int num_blocks, pa_dtype dtype,
+                         int *d_err, void *stream);
+
+/*
+ * pa_decode_partition_tokens -- the split-K partition length pa_decode uses
+ * for these arguments: partition_tokens itself when > 0, otherwise the
+ * automatic choice.  Returns 0 when the arguments are invalid.
+ */
+PA_API int pa_decode_partition_tokens(int num_seqs, int num_kv_heads, int block_size,
+                               int max_context_len, int partition_tokens);
+
+/*
+ * pa_decode_workspace_bytes -- device workspace pa_decode needs for split-K
+ * partials with these arguments (0 when every sequence fits one partition).
+ * Layout (internal): fp32 partial accumulators and (max, sum) pairs per
+ * (sequence, query head, partition).
+ */
+PA_API size_t pa_decode_workspace_bytes(int num_seqs, int num_heads, int head_dim, int block_size,
+                                 int max_context_len, int partition_tokens);
+
+/*
+ * pa_decode -- single-query paged attention (one decode step).
+ * For each sequence s and query head h, with L = context_lens[s] and
+ * kvh = h / (num_heads/num_kv_heads):
+ *   1. look up physical block block_tables[s][j / block_size] for j < L,
+ *   2. gather K and V rows from those blocks,
+ *   3. out[s][h] = sum_j softmax_j(scale * q[s][h] . K_j) V_j,
+ * accumulated in fp32 and rounded once to dtype (round to nearest even).
+ *
+ *   out            [num_seqs][num_heads][head_dim] dtype (written)
+ *   query          [num_seqs][num_heads][head_dim] dtype
+ *   block_tables   int32 [num_seqs][max_blocks_per_seq]; entries past
+ *                  ceil(L/block_size) are never read
+ *   context_lens   int32 [num_seqs], includes the newest token; 0 gives zeros
+ *   max_context_len  host upper bound on every context_lens[s]
+ *   partition_tokens 0 = automatic; otherwise a positive multiple of
+ *                  block_size: each sequence is split into partitions of this
+ *                  many tokens, attended independently, then merged by a
+ *                  log-sum-exp reduction (a second kernel on the same stream)
+ *   workspace      device buffer of >= pa_decode_workspace_bytes(...) bytes
+ *                  (may be NULL when that is 0); its contents are scratch
+ * Supported: head_dim in {64, 128}; block_size in {8, 16, 32};
+ *   num_heads / num_kv_heads in {1, 2, 4, 8}; dtype f16 or bf16.
+ * Invalid lengths are clamped to [0, min(max_context_len,
+ * max_blocks_per_seq*block_size)] and flagged; invalid table entries are
+ * flagged and their rows skipped.
+ */
+PA_API int pa_decode(void *out, const void *query, const void *k_cache, const void *v_cache,
+              const int32_t *block_tables, int max_blocks_per_seq, const int32_t *context_lens,
+              int num_seqs, int num_heads, int num_kv_heads, int head_dim, int block_size,
+              int num_blocks, int max_context_len, float scale, int partition_tokens,
+              pa_dtype dtype, void *workspace, size_t workspace_bytes, int *d_err,
+              void *stream);
+
+/*
+ * pa_copy_blocks -- copy-on-write: for each pair (src, dst) of `pairs`
+ * (int64 [num_pairs][2]), copy the whole K block and V block (all kv heads)
+ * of src to dst, bit-exact.  A pair is skipped and PA_DEVERR_COPY_PAIR set
+ * when an id is outside the pool, src == dst, its dst appears as another
+ * pair's dst, or its dst is any pair's src -- so the result never depends on
+ * the order in which pairs run.  Each pair costs an O(num_pairs) scan of the
+ * list on the device.
+ */
+PA_API int pa_copy_blocks(void *k_cache, void *v_cache, const int64_t *pairs, int num_pairs,
+                   int num_kv_heads, int head_dim, int block_size, int num_blocks,
+                   pa_dtype dtype, int *d_err, void *stream);
+
+/*
+ * pa_prefill_chunk -- attention of one prompt chunk over its sequence's paged
+ * KV, causal: row i (absolute position prefix_len + i) attends to keys
+ * 0 .. prefix_len + i.  The chunk's own K/V must already be in the cache
+ * (pa_reshape_and_cache).  Matmuls run on the tensor cores with fp32
+ * accumulation; output rounded once to dtype.
+ *
+ *   out    [chunk_len][num_heads][head_dim] dtype (written)
+ *   query  [chunk_len][num_heads][head_dim] dtype
+ *   block_table int32 [>= ceil((prefix_len+chunk_len)/block_size)]
+ * Supported: head_dim 128, block_size in {16, 32}, group size in {1,2,4,8},
+ * dtype f16 or bf16.
+ */
+PA_API int pa_prefill_chunk(void *out, const void *query, const void *k_cache, const void *v_cache,
+                     const int32_t *block_table, int prefix_len, int chunk_len, int num_heads,
+                     int num_kv_heads, int head_dim, int block_size, int num_blocks, float scale,
+                     pa_dtype dtype, int *d_err, void *stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PA_H */

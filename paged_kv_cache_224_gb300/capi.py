@@ -1,0 +1,185 @@
+"""Thin Python binding of the C ABI in ``include/pa.h`` (ctypes).
+
+Argument marshalling only: every function takes torch CUDA tensors, checks
+dtypes and shapes, passes raw device pointers and the current CUDA stream to
+the C entry point of the same name, and raises :class:`PAError` on a
+non-zero status.  All computation happens in the CUDA kernels of
+``libpa.so``; there is no fallback of any kind -- if the library cannot be
+loaded, every call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libpa.so")
+
+PA_F16, PA_BF16 = 0, 1
+DEVERR = {"slot_range": 0x1, "block_range": 0x2, "context_range": 0x4, "copy_pair": 0x8,
+          "timeout": 0x10}
+EXPORTED = ("pa_status_string", "pa_reshape_and_cache", "pa_decode_partition_tokens",
+            "pa_decode_workspace_bytes", "pa_decode", "pa_copy_blocks", "pa_prefill_chunk")
+
+_lib = None
+
+
+class PAError(RuntimeError):
+    def __init__(self, fn: str, status: int):
+        self.status = status
+        super().__init__(f"{fn} failed: {pa_status_string(status)} ({status})")
+
+
+def lib() -> ctypes.CDLL:
+    """Load ``libpa.so`` (built by ``build.py``); raise if it is missing."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"paged-KV CUDA library not built: {LIB_PATH} is missing "
+                               "(run paged_kv_cache_224_gb300.build.build())")
+        L = ctypes.CDLL(LIB_PATH)
+        p, i, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t
+        L.pa_status_string.argtypes = [i]
+        L.pa_status_string.restype = ctypes.c_char_p
+        L.pa_reshape_and_cache.argtypes = [p, p, p, p, p, i, i, i, i, i, i, p, p]
+        L.pa_reshape_and_cache.restype = i
+        L.pa_decode_partition_tokens.argtypes = [i, i, i, i, i]
+        L.pa_decode_partition_tokens.restype = i
+        L.pa_decode_workspace_bytes.argtypes = [i, i, i, i, i, i]
+        L.pa_decode_workspace_bytes.restype = sz
+        L.pa_decode.argtypes = [p, p, p, p, p, i, p, i, i, i, i, i, i, i, ctypes.c_float, i, i,
+                                p, sz, p, p]
+        L.pa_decode.restype = i
+        L.pa_copy_blocks.argtypes = [p, p, p, i, i, i, i, i, i, p, p]
+        L.pa_copy_blocks.restype = i
+        L.pa_prefill_chunk.argtypes = [p, p, p, p, p, i, i, i, i, i, i, i, ctypes.c_float, i, p, p]
+        L.pa_prefill_chunk.restype = i
+        _lib = L
+    return _lib
+
+
+def pa_status_string(status: int) -> str:
+    return lib().pa_status_string(int(status)).decode()
+
+
+def _dt(t: torch.Tensor) -> int:
+    if t.dtype == torch.float16:
+        return PA_F16
+    if t.dtype == torch.bfloat16:
+        return PA_BF16
+    raise TypeError(f"unsupported dtype {t.dtype}")
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    return ctypes.c_void_p(t.data_ptr()) if t is not None else ctypes.c_void_p(0)
+
+
+def _dev(*ts):
+    for t in ts:
+        if t is not None:
+            if not t.is_cuda:
+                raise ValueError("tensor must be on a CUDA device")
+            if not t.is_contiguous():
+                raise ValueError("tensor must be contiguous")
+
+
+def _stream(t: torch.Tensor, stream=None):
+    s = stream if stream is not None else torch.cuda.current_stream(t.device)
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _check(fn, rc):
+    if rc != 0:
+        raise PAError(fn, rc)
+
+
+def pa_reshape_and_cache(key, value, k_cache, v_cache, slot_mapping, d_err=None, stream=None):
+    """key/value [T][Hkv][D]; caches [NB][Hkv][bs][D]; slot_mapping int64 [T]."""
+    _dev(key, value, k_cache, v_cache, slot_mapping, d_err)
+    if slot_mapping.dtype != torch.int64:
+        raise TypeError("slot_mapping must be int64")
+    NB, Hkv, bs, D = k_cache.shape
+    T = key.shape[0]
+    if key.shape != (T, Hkv, D) or value.shape != key.shape or slot_mapping.shape != (T,):
+        raise ValueError("shape mismatch")
+    if not (key.dtype == value.dtype == k_cache.dtype == v_cache.dtype):
+        raise TypeError("dtype mismatch")
+    rc = lib().pa_reshape_and_cache(_ptr(key), _ptr(value), _ptr(k_cache), _ptr(v_cache),
+                                    _ptr(slot_mapping), T, Hkv, D, bs, NB, _dt(k_cache),
+                                    _ptr(d_err), _stream(k_cache, stream))
+    _check("pa_reshape_and_cache", rc)
+
+
+def pa_decode_partition_tokens(num_seqs, num_kv_heads, block_size, max_context_len,
+                               partition_tokens=0) -> int:
+    return lib().pa_decode_partition_tokens(num_seqs, num_kv_heads, block_size, max_context_len,
+                                            partition_tokens)
+
+
+def pa_decode_workspace_bytes(num_seqs, num_heads, head_dim, block_size, max_context_len,
+                              partition_tokens=0) -> int:
+    return lib().pa_decode_workspace_bytes(num_seqs, num_heads, head_dim, block_size,
+                                           max_context_len, partition_tokens)
+
+
+def decode_workspace(query, block_size, max_context_len, partition_tokens=0):
+    """Allocate (with torch) a workspace big enough for ``pa_decode``."""
+    B, Hq, D = query.shape
+    n = pa_decode_workspace_bytes(B, Hq, D, block_size, max_context_len, partition_tokens)
+    return torch.empty(max(n, 1), dtype=torch.uint8, device=query.device)
+
+
+def pa_decode(out, query, k_cache, v_cache, block_tables, context_lens, scale, max_context_len,
+              partition_tokens=0, workspace=None, d_err=None, stream=None):
+    """out/query [B][Hq][D]; caches [NB][Hkv][bs][D]; block_tables int32 [B][MB];
+    context_lens int32 [B].  ``workspace`` defaults to a fresh torch buffer."""
+    _dev(out, query, k_cache, v_cache, block_tables, context_lens, workspace, d_err)
+    if block_tables.dtype != torch.int32 or context_lens.dtype != torch.int32:
+        raise TypeError("block_tables and context_lens must be int32")
+    NB, Hkv, bs, D = k_cache.shape
+    B, Hq, Dq = query.shape
+    if Dq != D or out.shape != query.shape or block_tables.shape[0] != B or context_lens.shape != (B,):
+        raise ValueError("shape mismatch")
+    if not (out.dtype == query.dtype == k_cache.dtype == v_cache.dtype):
+        raise TypeError("dtype mismatch")
+    if workspace is None:
+        workspace = decode_workspace(query, bs, max_context_len, partition_tokens)
+    rc = lib().pa_decode(_ptr(out), _ptr(query), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables),
+                         block_tables.shape[1], _ptr(context_lens), B, Hq, Hkv, D, bs, NB,
+                         int(max_context_len), float(scale), int(partition_tokens), _dt(query),
+                         _ptr(workspace), workspace.numel() * workspace.element_size(),
+                         _ptr(d_err), _stream(query, stream))
+    _check("pa_decode", rc)
+
+
+def pa_copy_blocks(k_cache, v_cache, pairs, d_err=None, stream=None):
+    """pairs int64 [n][2] of (src, dst) physical block ids."""
+    _dev(k_cache, v_cache, pairs, d_err)
+    if pairs.dtype != torch.int64:
+        raise TypeError("pairs must be int64")
+    NB, Hkv, bs, D = k_cache.shape
+    n = pairs.shape[0] if pairs.numel() else 0
+    rc = lib().pa_copy_blocks(_ptr(k_cache), _ptr(v_cache), _ptr(pairs), n, Hkv, D, bs, NB,
+                              _dt(k_cache), _ptr(d_err), _stream(k_cache, stream))
+    _check("pa_copy_blocks", rc)
+
+
+def pa_prefill_chunk(out, query, k_cache, v_cache, block_table, prefix_len, scale, d_err=None,
+                     stream=None):
+    """out/query [C][Hq][D]; block_table int32 [>= ceil((P+C)/bs)]."""
+    _dev(out, query, k_cache, v_cache, block_table, d_err)
+    if block_table.dtype != torch.int32:
+        raise TypeError("block_table must be int32")
+    NB, Hkv, bs, D = k_cache.shape
+    C, Hq, Dq = query.shape
+    if Dq != D or out.shape != query.shape:
+        raise ValueError("shape mismatch")
+    if block_table.shape[0] * bs < prefix_len + C:
+        raise ValueError("block table too short for prefix + chunk")
+    rc = lib().pa_prefill_chunk(_ptr(out), _ptr(query), _ptr(k_cache), _ptr(v_cache),
+                                _ptr(block_table), int(prefix_len), C, Hq, Hkv, D, bs, NB,
+                                float(scale), _dt(query), _ptr(d_err), _stream(query, stream))
+    _check("pa_prefill_chunk", rc)

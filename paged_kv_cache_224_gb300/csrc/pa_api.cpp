@@ -1,0 +1,212 @@
+// C-ABI entry points: host-side argument validation, then kernel dispatch.
+// Nothing here allocates device memory or synchronises the stream.
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include <cmath>
+
+#include "../../include/pa.h"
+#include "pa_internal.h"
+
+namespace pa {
+int launch_decode_bf16(int head_dim, int block_size, int group, const DecodeParams &p,
+                       cudaStream_t stream);
+int launch_decode_f16(int head_dim, int block_size, int group, const DecodeParams &p,
+                      cudaStream_t stream);
+
+int launch_decode(pa_dtype dt, int head_dim, int block_size, int group, const DecodeParams &p,
+                  cudaStream_t stream) {
+    return dt == PA_BF16 ? launch_decode_bf16(head_dim, block_size, group, p, stream)
+                         : launch_decode_f16(head_dim, block_size, group, p, stream);
+}
+
+// Default split: 512-token partitions.  A sequence that fits one partition
+// is attended by a single CTA per kv head and needs no merge.
+int auto_partition_tokens(int num_seqs, int num_kv_heads, int block_size, int max_context_len) {
+    (void)num_seqs;
+    (void)num_kv_heads;
+    (void)max_context_len;
+    int pt = 512;
+    if (pt % block_size) pt = block_size;
+    return pt;
+}
+}  // namespace pa
+
+namespace {
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+bool good_dtype(pa_dtype d) { return d == PA_F16 || d == PA_BF16; }
+
+bool decode_shape_supported(int head_dim, int block_size, int group) {
+    return (head_dim == 64 || head_dim == 128) &&
+           (block_size == 8 || block_size == 16 || block_size == 32) &&
+           (group == 1 || group == 2 || group == 4 || group == 8);
+}
+
+int resolve_partition(int num_seqs, int num_kv_heads, int block_size, int max_context_len,
+                      int partition_tokens) {
+    if (partition_tokens < 0) return -1;
+    if (partition_tokens == 0)
+        return pa::auto_partition_tokens(num_seqs, num_kv_heads, block_size, max_context_len);
+    if (partition_tokens % block_size) return -1;
+    return partition_tokens;
+}
+
+int max_parts(int max_context_len, int pt) {
+    return max_context_len > 0 ? (max_context_len + pt - 1) / pt : 1;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char *pa_status_string(int status) {
+    switch (status) {
+    case PA_OK: return "PA_OK";
+    case PA_ERR_INVALID_ARG: return "PA_ERR_INVALID_ARG: null pointer, bad size or bad enum";
+    case PA_ERR_UNSUPPORTED: return "PA_ERR_UNSUPPORTED: no kernel for this shape";
+    case PA_ERR_OUT_OF_RANGE: return "PA_ERR_OUT_OF_RANGE: scalar argument out of range";
+    case PA_ERR_CUDA: return "PA_ERR_CUDA: CUDA runtime call failed";
+    case PA_ERR_WORKSPACE: return "PA_ERR_WORKSPACE: workspace missing or too small";
+    case PA_ERR_ALIGNMENT: return "PA_ERR_ALIGNMENT: pointer not 16-byte aligned";
+    default: return "unknown pa_status";
+    }
+}
+
+int pa_reshape_and_cache(const void *key, const void *value, void *k_cache, void *v_cache,
+                         const int64_t *slot_mapping, int num_tokens, int num_kv_heads,
+                         int head_dim, int block_size, int num_blocks, pa_dtype dtype, int *d_err,
+                         void *stream) {
+    if (num_tokens < 0 || num_kv_heads <= 0 || head_dim <= 0 || block_size <= 0 || num_blocks <= 0 ||
+        !good_dtype(dtype))
+        return PA_ERR_INVALID_ARG;
+    if (num_tokens == 0) return PA_OK;
+    if (!key || !value || !k_cache || !v_cache || !slot_mapping) return PA_ERR_INVALID_ARG;
+    if (head_dim % 8) return PA_ERR_UNSUPPORTED;
+    if (!aligned16(key) || !aligned16(value) || !aligned16(k_cache) || !aligned16(v_cache))
+        return PA_ERR_ALIGNMENT;
+    return pa::launch_reshape_and_cache(key, value, k_cache, v_cache, slot_mapping, num_tokens,
+                                        num_kv_heads, head_dim, block_size, num_blocks, d_err,
+                                        static_cast<cudaStream_t>(stream));
+}
+
+int pa_decode_partition_tokens(int num_seqs, int num_kv_heads, int block_size, int max_context_len,
+                               int partition_tokens) {
+    if (num_seqs < 0 || num_kv_heads <= 0 || block_size <= 0 || max_context_len < 0) return 0;
+    const int pt = resolve_partition(num_seqs, num_kv_heads, block_size, max_context_len,
+                                     partition_tokens);
+    return pt > 0 ? pt : 0;
+}
+
+size_t pa_decode_workspace_bytes(int num_seqs, int num_heads, int head_dim, int block_size,
+                                 int max_context_len, int partition_tokens) {
+    if (num_seqs <= 0 || num_heads <= 0 || head_dim <= 0 || block_size <= 0 || max_context_len < 0)
+        return 0;
+    const int pt = resolve_partition(num_seqs, 1, block_size, max_context_len, partition_tokens);
+    if (pt <= 0) return 0;
+    const int mp = max_parts(max_context_len, pt);
+    if (mp <= 1) return 0;
+    const size_t n = (size_t)num_seqs * num_heads * mp;
+    const size_t acc = (n * head_dim * sizeof(float) + 255) / 256 * 256;
+    return acc + n * 2 * sizeof(float);
+}
+
+int pa_decode(void *out, const void *query, const void *k_cache, const void *v_cache,
+              const int32_t *block_tables, int max_blocks_per_seq, const int32_t *context_lens,
+              int num_seqs, int num_heads, int num_kv_heads, int head_dim, int block_size,
+              int num_blocks, int max_context_len, float scale, int partition_tokens,
+              pa_dtype dtype, void *workspace, size_t workspace_bytes, int *d_err, void *stream) {
+    if (num_seqs < 0 || num_heads <= 0 || num_kv_heads <= 0 || head_dim <= 0 || block_size <= 0 ||
+        num_blocks <= 0 || max_blocks_per_seq <= 0 || max_context_len < 0 || !good_dtype(dtype))
+        return PA_ERR_INVALID_ARG;
+    if (num_heads % num_kv_heads) return PA_ERR_INVALID_ARG;
+    if (!std::isfinite(scale)) return PA_ERR_OUT_OF_RANGE;
+    if (num_seqs == 0) return PA_OK;
+    if (!out || !query || !k_cache || !v_cache || !block_tables || !context_lens)
+        return PA_ERR_INVALID_ARG;
+    const int group = num_heads / num_kv_heads;
+    if (!decode_shape_supported(head_dim, block_size, group)) return PA_ERR_UNSUPPORTED;
+    if (!aligned16(out) || !aligned16(query) || !aligned16(k_cache) || !aligned16(v_cache))
+        return PA_ERR_ALIGNMENT;
+    const int pt = resolve_partition(num_seqs, num_kv_heads, block_size, max_context_len,
+                                     partition_tokens);
+    if (pt <= 0) return PA_ERR_OUT_OF_RANGE;
+    const int mp = max_parts(max_context_len, pt);
+    pa::DecodeParams p{};
+    p.out = out;
+    p.query = query;
+    p.k_cache = k_cache;
+    p.v_cache = v_cache;
+    p.block_tables = block_tables;
+    p.context_lens = context_lens;
+    p.d_err = d_err;
+    p.num_seqs = num_seqs;
+    p.num_heads = num_heads;
+    p.num_kv_heads = num_kv_heads;
+    p.max_blocks_per_seq = max_blocks_per_seq;
+    p.num_blocks = num_blocks;
+    p.max_context_len = max_context_len;
+    p.block_size = block_size;
+    p.partition_tokens = pt;
+    p.max_partitions = mp;
+    p.scale_log2 = scale * 1.4426950408889634f;
+    if (mp > 1) {
+        const size_t need = pa_decode_workspace_bytes(num_seqs, num_heads, head_dim, block_size,
+                                                      max_context_len, pt);
+        if (!workspace || workspace_bytes < need) return PA_ERR_WORKSPACE;
+        if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return PA_ERR_ALIGNMENT;
+        const size_t n = (size_t)num_seqs * num_heads * mp;
+        const size_t acc = (n * head_dim * sizeof(float) + 255) / 256 * 256;
+        p.ws_acc = static_cast<float *>(workspace);
+        p.ws_ml = reinterpret_cast<float2 *>(static_cast<char *>(workspace) + acc);
+    }
+    return pa::launch_decode(dtype, head_dim, block_size, group, p,
+                             static_cast<cudaStream_t>(stream));
+}
+
+int pa_copy_blocks(void *k_cache, void *v_cache, const int64_t *pairs, int num_pairs,
+                   int num_kv_heads, int head_dim, int block_size, int num_blocks, pa_dtype dtype,
+                   int *d_err, void *stream) {
+    if (num_pairs < 0 || num_kv_heads <= 0 || head_dim <= 0 || block_size <= 0 || num_blocks <= 0 ||
+        !good_dtype(dtype))
+        return PA_ERR_INVALID_ARG;
+    if (num_pairs == 0) return PA_OK;
+    if (!k_cache || !v_cache || !pairs) return PA_ERR_INVALID_ARG;
+    if (((long long)num_kv_heads * block_size * head_dim) % 8) return PA_ERR_UNSUPPORTED;
+    if (!aligned16(k_cache) || !aligned16(v_cache)) return PA_ERR_ALIGNMENT;
+    return pa::launch_copy_blocks(k_cache, v_cache, pairs, num_pairs, num_kv_heads, head_dim,
+                                  block_size, num_blocks, d_err, static_cast<cudaStream_t>(stream));
+}
+
+int pa_prefill_chunk(void *out, const void *query, const void *k_cache, const void *v_cache,
+                     const int32_t *block_table, int prefix_len, int chunk_len, int num_heads,
+                     int num_kv_heads, int head_dim, int block_size, int num_blocks, float scale,
+                     pa_dtype dtype, int *d_err, void *stream) {
+    if (prefix_len < 0 || chunk_len < 0 || num_heads <= 0 || num_kv_heads <= 0 || head_dim <= 0 ||
+        block_size <= 0 || num_blocks <= 0 || !good_dtype(dtype))
+        return PA_ERR_INVALID_ARG;
+    if (num_heads % num_kv_heads) return PA_ERR_INVALID_ARG;
+    if (!std::isfinite(scale)) return PA_ERR_OUT_OF_RANGE;
+    if (chunk_len == 0) return PA_OK;
+    if (!out || !query || !k_cache || !v_cache || !block_table) return PA_ERR_INVALID_ARG;
+    if (!aligned16(out) || !aligned16(query) || !aligned16(k_cache) || !aligned16(v_cache))
+        return PA_ERR_ALIGNMENT;
+    pa::PrefillParams p{};
+    p.out = out;
+    p.query = query;
+    p.k_cache = k_cache;
+    p.v_cache = v_cache;
+    p.block_table = block_table;
+    p.d_err = d_err;
+    p.prefix_len = prefix_len;
+    p.chunk_len = chunk_len;
+    p.num_heads = num_heads;
+    p.num_kv_heads = num_kv_heads;
+    p.num_blocks = num_blocks;
+    p.scale_log2 = scale * 1.4426950408889634f;
+    return pa::launch_prefill(dtype, head_dim, block_size, num_heads / num_kv_heads, p,
+                              static_cast<cudaStream_t>(stream));
+}
+
+}  // extern "C"

@@ -1,0 +1,111 @@
+// Cache writes and copy-on-write block copies: pure data movement.
+//
+// reshape_and_cache follows the page "vLLM PagedAttention chuyen sau"
+// (locionic.com), section "Tuong tu phan trang bo nho ao": a growing sequence
+// gets new slots in its physical blocks; section "Chunked Prefill", step 3:
+// each chunk's KV accumulates in the same blocks.  copy_blocks follows
+// section "Co che APC", step 3: a shared block is copied before a sequence
+// that diverges writes into it.
+//
+// Both are HBM-bound streams of 16-byte vectors; every byte is moved once.
+#include "pa_device.cuh"
+#include "pa_internal.h"
+
+namespace pa {
+
+// One thread moves one 16-byte chunk of one (token, kv head) row for both K
+// and V.  Reads of key/value are fully coalesced; writes land as contiguous
+// head_dim*2-byte rows inside the destination tile.
+__global__ void __launch_bounds__(256)
+reshape_and_cache_kernel(const uint4 *__restrict__ key, const uint4 *__restrict__ value,
+                         uint4 *__restrict__ k_cache, uint4 *__restrict__ v_cache,
+                         const int64_t *__restrict__ slots, int num_tokens, int num_kv_heads,
+                         int chunks_per_row, int block_size, long long pool_slots, int *d_err) {
+    const long long per_token = (long long)num_kv_heads * chunks_per_row;
+    const long long total = per_token * num_tokens;
+    for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < total;
+         i += (long long)gridDim.x * blockDim.x) {
+        const long long t = i / per_token;
+        const long long r = i - t * per_token;  // = h * chunks_per_row + chunk
+        const int64_t slot = slots[t];
+        if (slot < 0) continue;                 // padding
+        if (slot >= pool_slots) {
+            if (r == 0) flag_error(d_err, PA_DEVERR_SLOT_RANGE);
+            continue;
+        }
+        const long long blk = slot / block_size;
+        const long long off = slot - blk * block_size;
+        const long long h = r / chunks_per_row;
+        const long long ch = r - h * chunks_per_row;
+        const long long dst = ((blk * num_kv_heads + h) * block_size + off) * chunks_per_row + ch;
+        k_cache[dst] = key[i];
+        v_cache[dst] = value[i];
+    }
+}
+
+int launch_reshape_and_cache(const void *key, const void *value, void *k_cache, void *v_cache,
+                             const int64_t *slots, int num_tokens, int num_kv_heads, int head_dim,
+                             int block_size, int num_blocks, int *d_err, cudaStream_t stream) {
+    const int cpr = head_dim / 8;
+    const long long total = (long long)num_tokens * num_kv_heads * cpr;
+    if (total == 0) return PA_OK;
+    long long blocks = (total + 255) / 256;
+    if (blocks > 152LL * 64) blocks = 152LL * 64;  // grid-stride beyond 64 CTAs per SM
+    reshape_and_cache_kernel<<<(unsigned)blocks, 256, 0, stream>>>(
+        static_cast<const uint4 *>(key), static_cast<const uint4 *>(value),
+        static_cast<uint4 *>(k_cache), static_cast<uint4 *>(v_cache), slots, num_tokens,
+        num_kv_heads, cpr, block_size, (long long)num_blocks * block_size, d_err);
+    return cudaPeekAtLastError() == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+}
+
+// grid = (num_pairs, pieces).  Each CTA first decides whether its pair is
+// valid by scanning the whole pair list (so every CTA of a pair reaches the
+// same verdict), then copies its piece of the K block and the V block.
+__global__ void __launch_bounds__(256)
+copy_blocks_kernel(uint4 *__restrict__ k_cache, uint4 *__restrict__ v_cache,
+                   const int64_t *__restrict__ pairs, int num_pairs, long long chunks_per_block,
+                   long long chunks_per_piece, int num_blocks, int *d_err) {
+    const int i = blockIdx.x;
+    const int64_t src = pairs[2 * i];
+    const int64_t dst = pairs[2 * i + 1];
+    bool ok = src >= 0 && src < num_blocks && dst >= 0 && dst < num_blocks && src != dst;
+    int conflict = 0;
+    for (int j = threadIdx.x; ok && j < num_pairs; j += blockDim.x) {
+        if ((j != i && pairs[2 * j + 1] == dst) || pairs[2 * j] == dst) conflict = 1;
+    }
+    ok = ok && !__syncthreads_or(conflict);
+    if (!ok) {
+        if (blockIdx.y == 0 && threadIdx.x == 0) flag_error(d_err, PA_DEVERR_COPY_PAIR);
+        return;
+    }
+    const long long begin = (long long)blockIdx.y * chunks_per_piece;
+    const long long end = min(begin + chunks_per_piece, chunks_per_block);
+    const uint4 *ks = k_cache + src * chunks_per_block;
+    const uint4 *vs = v_cache + src * chunks_per_block;
+    uint4 *kd = k_cache + dst * chunks_per_block;
+    uint4 *vd = v_cache + dst * chunks_per_block;
+    for (long long c = begin + threadIdx.x; c < end; c += blockDim.x) {
+        const uint4 a = ks[c];
+        const uint4 b = vs[c];
+        kd[c] = a;
+        vd[c] = b;
+    }
+}
+
+int launch_copy_blocks(void *k_cache, void *v_cache, const int64_t *pairs, int num_pairs,
+                       int num_kv_heads, int head_dim, int block_size, int num_blocks, int *d_err,
+                       cudaStream_t stream) {
+    if (num_pairs == 0) return PA_OK;
+    const long long cpb = (long long)num_kv_heads * block_size * head_dim / 8;
+    const long long per_piece = 256 * 4;  // 4 vectors per thread per cache
+    long long pieces = (cpb + per_piece - 1) / per_piece;
+    if (pieces > 65535) pieces = 65535;
+    const long long chunks_per_piece = (cpb + pieces - 1) / pieces;
+    dim3 grid((unsigned)num_pairs, (unsigned)pieces);
+    copy_blocks_kernel<<<grid, 256, 0, stream>>>(static_cast<uint4 *>(k_cache),
+                                                 static_cast<uint4 *>(v_cache), pairs, num_pairs,
+                                                 cpb, chunks_per_piece, num_blocks, d_err);
+    return cudaPeekAtLastError() == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+}
+
+}  // namespace pa

@@ -1,0 +1,55 @@
+// Host-side declarations shared by the C-ABI layer and the kernel files.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "../../include/pa.h"
+
+namespace pa {
+
+// Everything a decode launch needs; passed by value to the kernels.
+struct DecodeParams {
+    void *out;                   // [B][Hq][D] dtype
+    const void *query;           // [B][Hq][D] dtype
+    const void *k_cache;         // [NB][Hkv][bs][D]
+    const void *v_cache;
+    const int32_t *block_tables; // [B][MB]
+    const int32_t *context_lens; // [B]
+    float *ws_acc;               // [B][Hq][max_partitions][D] unnormalised partial sums
+    float2 *ws_ml;               // [B][Hq][max_partitions] (running max in log2 units, sum)
+    int *d_err;
+    int num_seqs, num_heads, num_kv_heads, max_blocks_per_seq, num_blocks, max_context_len;
+    int block_size, partition_tokens, max_partitions;
+    float scale_log2;            // scale * log2(e)
+};
+
+struct PrefillParams {
+    void *out;                   // [C][Hq][D]
+    const void *query;           // [C][Hq][D]
+    const void *k_cache;
+    const void *v_cache;
+    const int32_t *block_table;  // [>= ceil((P+C)/bs)]
+    int *d_err;
+    int prefix_len, chunk_len, num_heads, num_kv_heads, num_blocks;
+    float scale_log2;
+};
+
+// Split-K partition length for the automatic setting.
+int auto_partition_tokens(int num_seqs, int num_kv_heads, int block_size, int max_context_len);
+
+// Kernel launchers.  Each returns PA_OK, PA_ERR_UNSUPPORTED (no instance for
+// the shape) or PA_ERR_CUDA (launch / attribute failure).
+int launch_decode(pa_dtype dt, int head_dim, int block_size, int group, const DecodeParams &p,
+                  cudaStream_t stream);
+int launch_reshape_and_cache(const void *key, const void *value, void *k_cache, void *v_cache,
+                             const int64_t *slots, int num_tokens, int num_kv_heads, int head_dim,
+                             int block_size, int num_blocks, int *d_err, cudaStream_t stream);
+int launch_copy_blocks(void *k_cache, void *v_cache, const int64_t *pairs, int num_pairs,
+                       int num_kv_heads, int head_dim, int block_size, int num_blocks, int *d_err,
+                       cudaStream_t stream);
+int launch_prefill(pa_dtype dt, int head_dim, int block_size, int group, const PrefillParams &p,
+                   cudaStream_t stream);
+
+}  // namespace pa

@@ -1,0 +1,105 @@
+"""CPU-side checks of the C ABI: the library builds, loads, exports every
+symbol ``include/pa.h`` declares, and rejects bad arguments on the host
+without launching anything (no GPU needed for any of this)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from paged_kv_cache_224_gb300 import build
+    build.build()
+    import paged_kv_cache_224_gb300 as pa
+    return pa.lib()
+
+
+def declared_symbols():
+    text = open(os.path.join(ROOT, "include", "pa.h")).read()
+    return sorted(set(re.findall(r"PA_API\s+[\w\s\*]+?\b(pa_\w+)\s*\(", text)))
+
+
+def test_header_declares_the_entry_points():
+    names = declared_symbols()
+    for n in ("pa_reshape_and_cache", "pa_decode", "pa_copy_blocks", "pa_prefill_chunk",
+              "pa_decode_workspace_bytes", "pa_status_string"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for n in declared_symbols():
+        assert hasattr(lib, n), n
+    from paged_kv_cache_224_gb300 import capi
+    assert sorted(capi.EXPORTED) == sorted(declared_symbols())
+
+
+def test_status_strings(lib):
+    import paged_kv_cache_224_gb300 as pa
+    assert pa.pa_status_string(0) == "PA_OK"
+    assert "WORKSPACE" in pa.pa_status_string(-5)
+    assert "unknown" in pa.pa_status_string(1234)
+
+
+def test_workspace_and_partition_rules(lib):
+    import paged_kv_cache_224_gb300 as pa
+    # every sequence fits one partition -> no workspace
+    assert pa.pa_decode_workspace_bytes(4, 4, 64, 16, 64, 0) == 0
+    assert pa.pa_decode_partition_tokens(256, 8, 16, 4096, 0) == 512
+    n = pa.pa_decode_workspace_bytes(256, 32, 128, 16, 4096, 0)
+    parts = 8
+    assert n >= 256 * 32 * parts * (128 + 2) * 4
+    # explicit partitions must be multiples of block_size
+    assert pa.pa_decode_partition_tokens(4, 4, 16, 100, 24) == 0
+    assert pa.pa_decode_partition_tokens(4, 4, 16, 100, 32) == 32
+
+
+def call_decode(lib, **kw):
+    a = dict(out=1 << 20, query=1 << 20, k=1 << 20, v=1 << 20, bt=1 << 20, mb=4, lens=1 << 20, B=2,
+             Hq=8, Hkv=2, D=128, bs=16, NB=64, maxlen=64, scale=0.1, pt=0, dt=1, ws=None, wsb=0)
+    a.update(kw)
+    p = ctypes.c_void_p
+    return lib.pa_decode(p(a["out"]), p(a["query"]), p(a["k"]), p(a["v"]), p(a["bt"]), a["mb"],
+                         p(a["lens"]), a["B"], a["Hq"], a["Hkv"], a["D"], a["bs"], a["NB"], a["maxlen"],
+                         a["scale"], a["pt"], a["dt"], p(a["ws"]), a["wsb"], None, None)
+
+
+def test_decode_rejects_bad_arguments_on_host(lib):
+    # These return before any CUDA call, so no device is touched.
+    assert call_decode(lib, out=0) == -1                  # null pointer
+    assert call_decode(lib, Hq=7) == -1                   # Hq % Hkv != 0
+    assert call_decode(lib, D=96) == -2                   # unsupported head_dim
+    assert call_decode(lib, bs=64) == -2                  # unsupported block_size
+    assert call_decode(lib, Hq=32, Hkv=2) == -2           # group 16 unsupported
+    assert call_decode(lib, dt=7) == -1                   # bad dtype
+    assert call_decode(lib, query=(1 << 20) + 2) == -6    # misaligned
+    assert call_decode(lib, scale=float("inf")) == -3
+    assert call_decode(lib, pt=24) == -3                  # not a multiple of block_size
+    assert call_decode(lib, maxlen=5000) == -5            # split needs a workspace
+    assert call_decode(lib, B=0) == 0                     # nothing to do
+
+
+def test_cache_calls_reject_bad_arguments_on_host(lib):
+    p = ctypes.c_void_p
+    buf = p(1 << 20)
+    assert lib.pa_reshape_and_cache(buf, buf, buf, buf, None, 4, 2, 128, 16, 64, 1, None, None) == -1
+    assert lib.pa_reshape_and_cache(buf, buf, buf, buf, buf, 4, 2, 12, 16, 64, 1, None, None) == -2
+    assert lib.pa_reshape_and_cache(buf, buf, buf, buf, buf, 0, 2, 128, 16, 64, 1, None, None) == 0
+    assert lib.pa_copy_blocks(buf, None, buf, 3, 2, 128, 16, 64, 1, None, None) == -1
+    assert lib.pa_copy_blocks(buf, buf, buf, 0, 2, 128, 16, 64, 1, None, None) == 0
+    assert lib.pa_prefill_chunk(buf, buf, buf, buf, buf, 8, 4, 7, 2, 128, 16, 64, 0.1, 1, None, None) == -1
+
+
+def test_product_path_has_no_oracle_import():
+    # the package must not reach the CPU oracle (only tests, smoke and the
+    # benchmark's CPU legs may)
+    pkg = os.path.join(ROOT, "paged_kv_cache_224_gb300")
+    for dirpath, _, files in os.walk(pkg):
+        for f in files:
+            if f.endswith((".py", ".cu", ".cuh", ".cpp", ".h")):
+                text = open(os.path.join(dirpath, f)).read()
+                assert "import oracle" not in text and "from oracle" not in text, f
+                assert "oracle.c" not in text, f
