@@ -64,7 +64,8 @@ def test_opt13b_mha_full_size():
 
 def test_llama_gqa_full_size():
     c = wl.llama_gqa_case()
-    assert c.num_seqs == 256 and c.max_blocks_per_seq == 256
+    assert c.num_seqs == 256 and c.max_blocks_per_seq == wl.blocks_for(c.max_context_len, 16)
+    assert 1 <= c.context_lens.min() and c.context_lens.max() <= 4096
     full_step_and_check(c, k_samples=16)
 
 
