@@ -59,8 +59,12 @@ typedef enum {
     PA_ERR_OUT_OF_RANGE = -3,  /* a host scalar outside its allowed range */
     PA_ERR_CUDA = -4,          /* a CUDA runtime call failed (launch, attribute) */
     PA_ERR_WORKSPACE = -5,     /* workspace missing or smaller than required */
-    PA_ERR_ALIGNMENT = -6      /* a pointer is not 16-byte aligned */
+    PA_ERR_ALIGNMENT = -6,     /* a pointer is not 16-byte aligned */
+    PA_ERR_SCRATCH_LIMIT = -7  /* pa_decode_noalloc: partials exceed its fixed scratch array */
 } pa_status;
+
+/* Size of the device array pa_decode_noalloc keeps its split-K partials in. */
+#define PA_NOALLOC_SCRATCH_BYTES ((size_t)64 << 20)
 
 /* Bits OR-ed into *d_err by the kernels. */
 #define PA_DEVERR_SLOT_RANGE 0x1    /* slot_mapping entry >= num_blocks*block_size */
@@ -140,6 +144,39 @@ PA_API int pa_decode(void *out, const void *query, const void *k_cache, const vo
               int num_blocks, int max_context_len, float scale, int partition_tokens,
               pa_dtype dtype, void *workspace, size_t workspace_bytes, int *d_err,
               void *stream);
+
+/*
+ * pa_decode_noalloc -- pa_decode for callers that must not allocate device
+ * memory.  The pages have no counterpart; this exists for hosts that cannot
+ * call cudaMalloc on this path: an inference engine that has already handed
+ * nearly all HBM to its KV-cache pool (there is nothing left to allocate from,
+ * and a failed allocation mid-step is fatal), or a latency-critical loop that
+ * cannot afford the device-wide synchronisation cudaMalloc/cudaFree imply.
+ *
+ * Same arguments, results and errors as pa_decode, minus the workspace: the
+ * split-K partials go to one array of PA_NOALLOC_SCRATCH_BYTES (64 MiB) that
+ * the library declares as a static device variable.  Every GPU that loads the
+ * library holds that array until the process exits, whether or not this entry
+ * point is ever called.
+ *   - Sizes whose partials would not fit (pa_decode_workspace_bytes(...) >
+ *     PA_NOALLOC_SCRATCH_BYTES) return PA_ERR_SCRATCH_LIMIT and launch
+ *     nothing; use pa_decode with a caller-owned workspace, or a longer
+ *     partition_tokens, for those.
+ *   - The first call on each device looks up the array's device address
+ *     (cudaGetSymbolAddress) with that device current; make that first call
+ *     before any stream capture.
+ *   - All calls on a device share the one array.  Calls whose kernels can
+ *     overlap on the GPU (different streams, no ordering between them) race
+ *     on it and corrupt each other's results; serialise them.  The array
+ *     needs no clearing: every partial is written before it is read.
+ * Nothing here calls cudaMalloc, cudaFree or any allocating routine.
+ */
+PA_API int pa_decode_noalloc(void *out, const void *query, const void *k_cache, const void *v_cache,
+                             const int32_t *block_tables, int max_blocks_per_seq,
+                             const int32_t *context_lens, int num_seqs, int num_heads,
+                             int num_kv_heads, int head_dim, int block_size, int num_blocks,
+                             int max_context_len, float scale, int partition_tokens,
+                             pa_dtype dtype, int *d_err, void *stream);
 
 /*
  * pa_copy_blocks -- copy-on-write: for each pair (src, dst) of `pairs`

@@ -22,7 +22,10 @@ PA_F16, PA_BF16 = 0, 1
 DEVERR = {"slot_range": 0x1, "block_range": 0x2, "context_range": 0x4, "copy_pair": 0x8,
           "timeout": 0x10}
 EXPORTED = ("pa_status_string", "pa_reshape_and_cache", "pa_decode_partition_tokens",
-            "pa_decode_workspace_bytes", "pa_decode", "pa_copy_blocks", "pa_prefill_chunk")
+            "pa_decode_workspace_bytes", "pa_decode", "pa_copy_blocks", "pa_prefill_chunk",
+            "pa_decode_noalloc")
+PA_ERR_SCRATCH_LIMIT = -7
+NOALLOC_SCRATCH_BYTES = 64 << 20
 
 _lib = None
 
@@ -53,6 +56,9 @@ def lib() -> ctypes.CDLL:
         L.pa_decode.argtypes = [p, p, p, p, p, i, p, i, i, i, i, i, i, i, ctypes.c_float, i, i,
                                 p, sz, p, p]
         L.pa_decode.restype = i
+        L.pa_decode_noalloc.argtypes = [p, p, p, p, p, i, p, i, i, i, i, i, i, i, ctypes.c_float,
+                                        i, i, p, p]
+        L.pa_decode_noalloc.restype = i
         L.pa_copy_blocks.argtypes = [p, p, p, i, i, i, i, i, i, p, p]
         L.pa_copy_blocks.restype = i
         L.pa_prefill_chunk.argtypes = [p, p, p, p, p, i, i, i, i, i, i, i, ctypes.c_float, i, p, p]
@@ -153,6 +159,27 @@ def pa_decode(out, query, k_cache, v_cache, block_tables, context_lens, scale, m
                          _ptr(workspace), workspace.numel() * workspace.element_size(),
                          _ptr(d_err), _stream(query, stream))
     _check("pa_decode", rc)
+
+
+def pa_decode_noalloc(out, query, k_cache, v_cache, block_tables, context_lens, scale,
+                      max_context_len, partition_tokens=0, d_err=None, stream=None):
+    """``pa_decode`` without a workspace: the split-K partials go to the
+    library's fixed device scratch array (``NOALLOC_SCRATCH_BYTES``).  Raises
+    PAError(PA_ERR_SCRATCH_LIMIT) for sizes that do not fit."""
+    _dev(out, query, k_cache, v_cache, block_tables, context_lens, d_err)
+    if block_tables.dtype != torch.int32 or context_lens.dtype != torch.int32:
+        raise TypeError("block_tables and context_lens must be int32")
+    NB, Hkv, bs, D = k_cache.shape
+    B, Hq, Dq = query.shape
+    if Dq != D or out.shape != query.shape or block_tables.shape[0] != B or context_lens.shape != (B,):
+        raise ValueError("shape mismatch")
+    if not (out.dtype == query.dtype == k_cache.dtype == v_cache.dtype):
+        raise TypeError("dtype mismatch")
+    rc = lib().pa_decode_noalloc(_ptr(out), _ptr(query), _ptr(k_cache), _ptr(v_cache),
+                                 _ptr(block_tables), block_tables.shape[1], _ptr(context_lens), B, Hq,
+                                 Hkv, D, bs, NB, int(max_context_len), float(scale),
+                                 int(partition_tokens), _dt(query), _ptr(d_err), _stream(query, stream))
+    _check("pa_decode_noalloc", rc)
 
 
 def pa_copy_blocks(k_cache, v_cache, pairs, d_err=None, stream=None):

@@ -70,6 +70,8 @@ const char *pa_status_string(int status) {
     case PA_ERR_CUDA: return "PA_ERR_CUDA: CUDA runtime call failed";
     case PA_ERR_WORKSPACE: return "PA_ERR_WORKSPACE: workspace missing or too small";
     case PA_ERR_ALIGNMENT: return "PA_ERR_ALIGNMENT: pointer not 16-byte aligned";
+    case PA_ERR_SCRATCH_LIMIT:
+        return "PA_ERR_SCRATCH_LIMIT: split-K partials exceed the fixed scratch of pa_decode_noalloc";
     default: return "unknown pa_status";
     }
 }
