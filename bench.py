@@ -155,7 +155,11 @@ def make_case(name: str, seed_offset: int):
     if name == "opt13b_mha":
         return wl.opt13b_case(seed=1001 + seed_offset)
     if name == "long_context":
-        return wl.long_context_case(seed=1004 + seed_offset)
+        return wl.long_context_case(block_size=16, seed=1004 + seed_offset)
+    if name == "long_context_bs32":
+        return wl.long_context_case(block_size=32, seed=1004 + seed_offset)
+    if name == "shared_prefix":
+        return wl.shared_prefix_case(seed=1003 + seed_offset)
     raise SystemExit(f"unknown workload {name}")
 
 
@@ -217,7 +221,8 @@ def main():
     ap.add_argument("--steps", type=int, default=500)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--workload", default="llama_gqa", choices=["llama_gqa", "opt13b_mha", "long_context"])
+    ap.add_argument("--workload", default="llama_gqa", choices=["llama_gqa", "opt13b_mha", "long_context", "long_context_bs32",
+                             "shared_prefix"])
     ap.add_argument("--partition-tokens", type=int, default=0)
     ap.add_argument("--e2e-steps", type=int, default=50)
     ap.add_argument("--cpu-seqs", type=int, default=64, help="sequences in the CPU-baseline sample")
@@ -262,9 +267,16 @@ def main():
     part = pa.pa_decode_partition_tokens(case.num_seqs, case.num_kv_heads, case.block_size,
                                          case.max_context_len, pt)
     max_parts = -(-case.max_context_len // part)
-    launches_per_step = 1 + 1 + (1 if max_parts > 1 else 0)
+    pairs = torch.as_tensor(case.cow_pairs, device=dev) if case.cow_pairs.shape[0] else None
+    launches_per_step = (1 if pairs is not None else 0) + 1 + 1 + (1 if max_parts > 1 else 0)
+
+    def cow():
+        # copy-on-write of shared blocks before the tails are written (idempotent across steps)
+        if pairs is not None:
+            pa.pa_copy_blocks(t["k_cache"], t["v_cache"], pairs, d_err=err)
 
     def step():
+        cow()
         pa.pa_reshape_and_cache(t["new_key"], t["new_value"], t["k_cache"], t["v_cache"], slots, d_err=err)
         pa.pa_decode(out, t["query"], t["k_cache"], t["v_cache"], bt, lens, case.scale,
                      case.max_context_len, partition_tokens=pt, workspace=ws, d_err=err)
@@ -285,6 +297,7 @@ def main():
         stop = torch.cuda.Event(enable_timing=True)
         start.record(stream)
         for i in range(args.steps):
+            cow()
             pa.pa_reshape_and_cache(t["new_key"], t["new_value"], t["k_cache"], t["v_cache"], slots, d_err=err)
             ev[i][0].record(stream)
             pa.pa_decode(out, t["query"], t["k_cache"], t["v_cache"], bt, lens, case.scale,
@@ -297,7 +310,7 @@ def main():
     decode_ms = [a.elapsed_time(b) for a, b in ev]
     elapsed_ms = max_over_ranks(elapsed_ms, world, dev)
 
-    step_bytes = case.decode_bytes() + case.reshape_bytes()
+    step_bytes = case.decode_bytes() + case.reshape_bytes() + case.copy_bytes()
     total_bytes = sum_over_ranks(float(step_bytes) * args.steps, world, dev)
     gbs = total_bytes / (elapsed_ms / 1e3) / 1e9
     ms_per_step = elapsed_ms / args.steps
@@ -325,6 +338,7 @@ def main():
     def e2e_step():
         for d, h in ((d_q, h_q), (d_nk, h_nk), (d_nv, h_nv), (d_slots, h_slots), (d_bt, h_bt), (d_lens, h_lens)):
             d.copy_(h, non_blocking=True)
+        cow()
         pa.pa_reshape_and_cache(d_nk, d_nv, t["k_cache"], t["v_cache"], d_slots, d_err=err)
         pa.pa_decode(out, d_q, t["k_cache"], t["v_cache"], d_bt, d_lens, case.scale,
                      case.max_context_len, partition_tokens=pt, workspace=ws, d_err=err)
@@ -361,7 +375,8 @@ def main():
                        "l2": "inputs larger than L2: KV pool %.2f GB, %.2f GB read per step" % (
                            2 * case.num_blocks * case.num_kv_heads * case.block_size * case.head_dim * 2 / 1e9,
                            case.kv_bytes() / 1e9),
-                       "step": "pa_reshape_and_cache (1 token/seq) + pa_decode",
+                       "step": ("pa_copy_blocks + " if pairs is not None else "")
+                               + f"pa_reshape_and_cache ({case.num_new_tokens} tokens) + pa_decode",
                        "parallelism": f"replicas x{world}, sequences sharded, no collective"},
             "pct_of_peak": round(100 * gbs / peak, 2),
             "tokens_per_s": round(tokens_per_s, 1),
