@@ -1,0 +1,114 @@
+"""GPU parity of chunked prefill against the CPU oracle, through the C ABI.
+
+A chunk of C query rows at positions P..P+C-1 attends causally over the
+paged prefix plus itself (page "vLLM PagedAttention chuyen sau", section
+"Chunked Prefill").  Checked: small ragged cases against the oracle in full,
+the full 8192-token-prefix / 512-token-chunk workload on sampled rows (the
+oracle's prefill row i equals its decode at context P+i+1, a pinned
+identity), and the pages' "KV accumulates chunk by chunk" invariant: writing
+a prompt's K/V chunk by chunk leaves the cache bit-identical to one write.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import paged_kv_cache_224_gb300 as pa
+from paged_kv_cache_224_gb300 import workload as wl
+from tests.helpers import check_attention, to_f64
+
+pytestmark = pytest.mark.gpu
+DEV = torch.device("cuda:0") if torch.cuda.is_available() else None
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    import __graft_entry__ as g
+    g.build()
+
+
+def run_prefill(case, t):
+    err = torch.zeros(1, dtype=torch.int32, device=DEV)
+    pa.pa_reshape_and_cache(t["new_key"], t["new_value"], t["k_cache"], t["v_cache"],
+                            torch.as_tensor(case.slot_mapping, device=DEV), d_err=err)
+    out = torch.full_like(t["query"], float("nan"))
+    pa.pa_prefill_chunk(out, t["query"], t["k_cache"], t["v_cache"],
+                        torch.as_tensor(case.block_table, device=DEV), case.prefix_len, case.scale, d_err=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0, f"device error flags {int(err.item()):#x}"
+    return out
+
+
+CASES = [
+    # (P, C, G, Hkv, bs, dtype)
+    (40, 9, 2, 2, 16, "bf16"),
+    (0, 17, 4, 1, 32, "f16"),
+    (100, 64, 8, 2, 16, "bf16"),
+    (333, 77, 1, 3, 16, "f16"),
+    (1000, 130, 4, 2, 32, "bf16"),
+    (64, 1, 8, 1, 16, "bf16"),
+]
+
+
+@pytest.mark.parametrize("P,C,G,Hkv,bs,dtype", CASES)
+def test_prefill_chunk_matches_oracle(P, C, G, Hkv, bs, dtype):
+    case = wl.make_prefill_case(f"pf{P}_{C}", P, C, G * Hkv, Hkv, 128, bs, dtype, seed=P + 7 * C + G)
+    t = case.materialize(DEV)
+    kc, vc = wl.bits(t["k_cache"]), wl.bits(t["v_cache"])
+    assert oracle.reshape_and_cache(wl.bits(t["new_key"]), wl.bits(t["new_value"]), kc, vc,
+                                    case.slot_mapping, bs) == 0
+    ref = oracle.prefill_chunk(wl.bits(t["query"]), kc, vc, case.block_table, P, case.scale, dtype,
+                               num_threads=8)
+    out = run_prefill(case, t)
+    check_attention(to_f64(out), ref, dtype, case.name)
+
+
+def test_prefill_full_size_sampled_rows():
+    case = wl.chunked_prefill_case()
+    assert (case.prefix_len, case.chunk_len, case.num_heads, case.num_kv_heads) == (8192, 512, 64, 8)
+    t = case.materialize(DEV)
+    n = wl.blocks_for(case.prefix_len + case.chunk_len, case.block_size)
+    idx = torch.as_tensor(case.block_table[:n], dtype=torch.long, device=DEV)
+    kc = wl.bits(t["k_cache"].index_select(0, idx))
+    vc = wl.bits(t["v_cache"].index_select(0, idx))
+    compact = np.arange(n, dtype=np.int32)
+    pos = np.arange(case.prefix_len, case.prefix_len + case.chunk_len)
+    slots = compact[pos // case.block_size].astype(np.int64) * case.block_size + pos % case.block_size
+    assert oracle.reshape_and_cache(wl.bits(t["new_key"]), wl.bits(t["new_value"]), kc, vc, slots,
+                                    case.block_size) == 0
+    q = wl.bits(t["query"])
+    out = run_prefill(case, t)
+    rows = [0, 1, 63, 64, 255, 300, 511]
+    for i in rows:
+        L = np.array([case.prefix_len + i + 1], np.int32)
+        ref = oracle.decode(q[i:i + 1], kc, vc, compact[None, :], L, case.scale, case.dtype, num_threads=8)
+        check_attention(to_f64(out[i:i + 1]), ref, case.dtype, f"row {i}")
+
+
+def test_prefill_row_equals_gpu_decode_at_that_position():
+    case = wl.make_prefill_case("pd", 500, 40, 8, 2, 128, 16, "bf16", seed=9)
+    t = case.materialize(DEV)
+    out = run_prefill(case, t)
+    bt = torch.as_tensor(case.block_table[None, :], device=DEV)
+    for i in (0, 17, 39):
+        dec = torch.empty_like(t["query"][i:i + 1])
+        L = torch.tensor([case.prefix_len + i + 1], dtype=torch.int32, device=DEV)
+        pa.pa_decode(dec, t["query"][i:i + 1].contiguous(), t["k_cache"], t["v_cache"], bt, L, case.scale,
+                     case.prefix_len + i + 1)
+        torch.cuda.synchronize()
+        assert (dec.float() - out[i:i + 1].float()).abs().max().item() <= 1e-2
+
+
+def test_chunkwise_cache_writes_are_bit_identical_to_one_write():
+    case = wl.make_prefill_case("acc", 0, 300, 4, 2, 128, 16, "bf16", seed=3)
+    t = case.materialize(DEV)
+    slots = torch.as_tensor(case.slot_mapping, device=DEV)
+    kc1, vc1 = t["k_cache"].clone(), t["v_cache"].clone()
+    pa.pa_reshape_and_cache(t["new_key"], t["new_value"], kc1, vc1, slots)
+    kc2, vc2 = t["k_cache"].clone(), t["v_cache"].clone()
+    for a in range(0, 300, 64):
+        b = min(300, a + 64)
+        pa.pa_reshape_and_cache(t["new_key"][a:b].contiguous(), t["new_value"][a:b].contiguous(), kc2, vc2,
+                                slots[a:b].contiguous())
+    torch.cuda.synchronize()
+    assert torch.equal(kc1, kc2) and torch.equal(vc1, vc2)
