@@ -34,6 +34,7 @@ import torch  # noqa: E402
 
 METRIC = "paged decode attention: achieved HBM GB/s (% of GB300 peak) and tokens/s"
 FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS = 1900.0
 
 
 def load_peaks():
@@ -215,6 +216,73 @@ def run_reference(args, world, rank):
     print(json.dumps(line), flush=True)
 
 
+def run_prefill_bench(args, world, rank, local, dev, stream):
+    """One chunked-prefill step: write the chunk's K/V (pa_reshape_and_cache),
+    then attend the 512-row chunk over its 8192-token paged prefix."""
+    import paged_kv_cache_224_gb300 as pa
+    from paged_kv_cache_224_gb300 import workload as wl
+    case = wl.chunked_prefill_case(seed=1004 + rank)
+    t = case.materialize(dev)
+    slots = torch.as_tensor(case.slot_mapping, device=dev)
+    bt = torch.as_tensor(case.block_table, device=dev)
+    out = torch.empty_like(t["query"])
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+
+    def step():
+        pa.pa_reshape_and_cache(t["new_key"], t["new_value"], t["k_cache"], t["v_cache"], slots, d_err=err)
+        pa.pa_prefill_chunk(out, t["query"], t["k_cache"], t["v_cache"], bt, case.prefix_len, case.scale,
+                            d_err=err)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    if int(err.item()) != 0:
+        raise SystemExit(f"device error flags {int(err.item()):#x}")
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    barrier(world)
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk:
+        start = torch.cuda.Event(enable_timing=True)
+        stop = torch.cuda.Event(enable_timing=True)
+        start.record(stream)
+        for i in range(args.steps):
+            pa.pa_reshape_and_cache(t["new_key"], t["new_value"], t["k_cache"], t["v_cache"], slots, d_err=err)
+            ev[i][0].record(stream)
+            pa.pa_prefill_chunk(out, t["query"], t["k_cache"], t["v_cache"], bt, case.prefix_len, case.scale,
+                                d_err=err)
+            ev[i][1].record(stream)
+        stop.record(stream)
+        torch.cuda.synchronize()
+    barrier(world)
+    elapsed_ms = max_over_ranks(start.elapsed_time(stop), world, dev)
+    flops = case.flops()
+    total = sum_over_ranks(float(flops) * args.steps, world, dev)
+    tflops = total / (elapsed_ms / 1e3) / 1e12
+    pf_ms = statistics.mean(a.elapsed_time(b) for a, b in ev)
+    achieved = flops / (pf_ms / 1e3) / 1e12
+    peak, kind = FALLBACK_BF16_TFLOPS, "fallback"
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        peak, kind = float(json.load(open(path))["bf16_tflops"]), "measured"
+    if rank == 0:
+        line = {"metric": "chunked prefill attention: achieved TFLOP/s (% of bf16 dense peak)",
+                "value": round(tflops, 2), "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+                "warmup": args.warmup, "ms_per_step": round(elapsed_ms / args.steps, 5),
+                "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": case.dtype,
+                "data": "synthetic",
+                "config": {"workload": case.name, "prefix_len": case.prefix_len, "chunk_len": case.chunk_len,
+                           "num_heads": case.num_heads, "num_kv_heads": case.num_kv_heads,
+                           "head_dim": case.head_dim, "block_size": case.block_size,
+                           "step": "pa_reshape_and_cache (chunk K/V) + pa_prefill_chunk",
+                           "l2": "KV of one kv head (4.5 MB) is reused from L2 by its row tiles"},
+                "roofline": {"bound": "tensor", "achieved": round(achieved, 2), "peak": peak,
+                             "unit": "TFLOP/s", "frac": round(achieved / peak, 4), "traffic": None,
+                             "kernel": "prefill_kernel", "flops_per_launch": flops, "avg_ms": round(pf_ms, 5),
+                             "peak_kind": f"{kind} (bf16 dense, burst)"},
+                "gpu_launches": 2 * args.steps, "clocks": clk.summary()}
+        print(json.dumps(line), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -222,7 +290,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="llama_gqa", choices=["llama_gqa", "opt13b_mha", "long_context", "long_context_bs32",
-                             "shared_prefix"])
+                             "shared_prefix", "chunked_prefill"])
     ap.add_argument("--partition-tokens", type=int, default=0)
     ap.add_argument("--e2e-steps", type=int, default=50)
     ap.add_argument("--cpu-seqs", type=int, default=64, help="sequences in the CPU-baseline sample")
@@ -248,6 +316,12 @@ def main():
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
     stream = torch.cuda.current_stream(dev)
+    if args.workload == "chunked_prefill":
+        run_prefill_bench(args, world, rank, local, dev, stream)
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+        return
 
     case = make_case(args.workload, rank)
     t = case.materialize(dev)
