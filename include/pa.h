@@ -195,8 +195,10 @@ PA_API int pa_copy_blocks(void *k_cache, void *v_cache, const int64_t *pairs, in
  * pa_prefill_chunk -- attention of one prompt chunk over its sequence's paged
  * KV, causal: row i (absolute position prefix_len + i) attends to keys
  * 0 .. prefix_len + i.  The chunk's own K/V must already be in the cache
- * (pa_reshape_and_cache).  Matmuls run on the tensor cores with fp32
- * accumulation; output rounded once to dtype.
+ * (pa_reshape_and_cache).  QK^T and PV run on the 5th-generation tensor cores
+ * (tcgen05.mma, accumulators in TMEM) with fp32 accumulation; P is rounded
+ * to dtype for the PV product;
+ * the output is rounded once to dtype.
  *
  *   out    [chunk_len][num_heads][head_dim] dtype (written)
  *   query  [chunk_len][num_heads][head_dim] dtype

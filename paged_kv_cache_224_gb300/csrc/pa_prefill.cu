@@ -1,314 +1,451 @@
-// Chunked-prefill attention over a paged KV cache (tensor cores).
+// Chunked-prefill attention on the 5th-generation tensor cores (tcgen05).
 //
 // Follows the page "vLLM PagedAttention chuyen sau" (locionic.com), section
-// "Chunked Prefill": a long prompt is processed chunk by chunk, each chunk's
-// KV accumulates in the sequence's blocks, and each chunk attends to the
-// cache built so far.  Query row i of the chunk sits at absolute position
-// prefix_len + i and attends causally to keys 0 .. prefix_len + i, gathered
-// through the block table exactly as in decode.
+// "Chunked Prefill": each chunk of a long prompt attends to the sequence's
+// paged cache built so far.  Query row i of the chunk sits at position
+// prefix_len + i and sees keys 0 .. prefix_len + i, gathered through the
+// block table.
 //
-// Unlike decode, a chunk against its keys is a dense contraction (C query
-// rows x G heads against every key), so QK^T and PV run on the tensor cores:
-// m16n8k16 MMAs with fp32 accumulation.  A CTA takes 64 (position, head)
-// rows of one kv head -- 64/G chunk positions times the G heads that share
-// the kv head -- so every K/V tile staged in shared memory serves all G heads.
-// Each of its 4 warps owns 16 rows; the Q fragments stay in registers for the
-// whole key loop.  K/V tiles of 64 keys are gathered row by row through the
-// block table with 16-byte cp.async copies into an XOR-swizzled layout
-// (conflict-free ldmatrix), double-buffered.  Softmax is online in fp32 (log2
-// units); P is rounded to the MMA input type for PV, as in any tensor-core
-// attention.  Keys past the causal limit of a row are masked; rows past the
-// chunk are not stored.
+// One CTA computes 128 query rows -- 128/G chunk positions times the G query
+// heads of one kv head -- against 128-key tiles:
+//   warp 0    TMA producer: for each key tile, one 2-D tensor copy per
+//             (block, 64-dim half) of K and of V, straight from the paged pool
+//             into a 128-byte-swizzled shared layout (two stages);
+//   warp 1    MMA issuer (one thread): S = Q K^T into TMEM (two buffers), then
+//             O += P V into TMEM, tcgen05.mma kind::f16, fp32 accumulation;
+//   warps 2-5 softmax: each thread owns one query row = one TMEM lane; reads
+//             its S row, applies the causal mask, updates the running max
+//             (rescaling O in TMEM only when the max grows by more than 2^8),
+//             writes P (rounded to the input type) into shared memory for the
+//             PV MMA, and finally normalises O and stores the row.
+// All waits are bounded; a wait that gives up flags PA_DEVERR_TIMEOUT.
+#include <cuda.h>
+
+#include <type_traits>
+
 #include "pa_device.cuh"
 #include "pa_internal.h"
 
 namespace pa {
 namespace {
 
-constexpr int kD = 128;         // head_dim supported by this kernel
-constexpr int kRows = 64;       // (position, head) rows per CTA
-constexpr int kKeys = 64;       // keys per K/V tile
-constexpr int kWarps = 4;
-constexpr int kThreads = kWarps * 32;
-constexpr int kRowBytes = kD * 2;                   // 256 bytes per row
-constexpr int kTileBytes = kKeys * kRowBytes;       // 16 KB per K or V tile
-constexpr int kQBytes = kRows * kRowBytes;          // 16 KB
-constexpr int kSmem = kQBytes + 2 * 2 * kTileBytes; // Q + double-buffered K and V = 80 KB
+constexpr int kD = 128;                     // head_dim
+constexpr int kM = 128;                     // query rows per CTA
+constexpr int kNK = 128;                    // keys per tile
+constexpr int kHalfBytes = 128 * 128;       // 128 rows x 64 elements x 2 bytes
+constexpr int kTileBytes = 2 * kHalfBytes;  // 32 KB: one operand tile (two 64-dim halves)
+constexpr int kOffQ = 0;
+constexpr int kOffKV = kOffQ + kTileBytes;                 // stage s: K at +64 KB*s, V after it
+constexpr int kStageBytes = 2 * kTileBytes;
+constexpr int kOffP = kOffKV + 2 * kStageBytes;            // 160 KB
+constexpr int kOffBar = kOffP + kTileBytes;                // 192 KB
+constexpr int kSmemUsed = kOffBar + 128;
+constexpr int kSmemAlloc = kSmemUsed + 1024;               // room to align the base to 1 KB
+constexpr int kThreads = 192;
+constexpr uint32_t kTmemCols = 512;                        // S0, S1, O (128 columns each)
 
-// Byte offset of 16-byte chunk `ch` (0..15) of row `r` in a swizzled tile:
-// the low three bits of the chunk index are XOR-ed with the row, so the 8
-// rows an ldmatrix reads at one logical chunk hit 8 different bank groups.
-__device__ __forceinline__ int swz(int r, int ch) { return r * kRowBytes + ((ch ^ (r & 7)) << 4); }
+// ---- tcgen05 / TMA wrappers (inline PTX) ---------------------------------
 
-__device__ __forceinline__ void cp_async16(uint32_t dst, const void *src, bool valid) {
-    const int n = valid ? 16 : 0;  // 0 source bytes -> 16 zero bytes
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(n) : "memory");
-}
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-template <int N>
-__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
 
-__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t (&r)[4]) {
-    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
-                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
-                 : "r"(addr));
-}
-__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t (&r)[4]) {
-    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
-                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
-                 : "r"(addr));
+// Shared-memory matrix descriptor: start, leading / stride byte offsets,
+// descriptor version 1, 128-byte swizzle.
+__device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+    uint64_t d = (uint64_t)((saddr >> 4) & 0x3FFF);
+    d |= (uint64_t)((lbo >> 4) & 0x3FFF) << 16;
+    d |= (uint64_t)((sbo >> 4) & 0x3FFF) << 32;
+    d |= (uint64_t)1 << 46;
+    d |= (uint64_t)2 << 61;
+    return d;
 }
 
-template <typename T> struct Mma;
-template <> struct Mma<__nv_bfloat16> {
-    static __device__ __forceinline__ void run(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
-                                               uint32_t b1) {
-        asm volatile(
-            "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
-            "{%0,%1,%2,%3};"
-            : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-            : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
-    }
-};
-template <> struct Mma<__half> {
-    static __device__ __forceinline__ void run(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
-                                               uint32_t b1) {
-        asm volatile(
-            "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
-            "{%0,%1,%2,%3};"
-            : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-            : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
-    }
-};
+// Instruction descriptor, kind::f16: fp32 accumulator, A and B both fp16 or
+// both bf16, A K-major, B K-major or MN-major, M = N = 128.
+__host__ __device__ constexpr uint32_t instr_desc(bool bf16, bool b_mn_major) {
+    return (1u << 4) | ((bf16 ? 1u : 0u) << 7) | ((bf16 ? 1u : 0u) << 10) |
+           ((b_mn_major ? 1u : 0u) << 16) | ((uint32_t)(128 >> 3) << 17) | ((uint32_t)(128 >> 4) << 24);
+}
 
-// Stage keys [k0, k0 + kKeys) of kv head kvh into a swizzled K tile and V tile.
-// Rows past `kend` (the last key any row of this CTA may see) are zero-filled
-// and never read from the cache; table entries outside the pool are flagged
-// and their rows zero-filled.
-template <int BS>
-__device__ __forceinline__ void load_kv_tile(const PrefillParams &p, uint32_t ks, uint32_t vs, int k0,
-                                             int kend, int kvh, const int32_t *__restrict__ table) {
-    const unsigned char *kc = static_cast<const unsigned char *>(p.k_cache);
-    const unsigned char *vc = static_cast<const unsigned char *>(p.v_cache);
-    // 64 rows x 16 chunks = 1024 chunks for K (and V); 8 per thread
+__device__ __forceinline__ void mma_f16(uint32_t tmem_d, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                        bool accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(tmem_d),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"((uint32_t)accumulate)
+        : "memory");
+}
+
+__device__ __forceinline__ void mma_commit(uint64_t *bar) {
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+                     smem_addr(bar))
+                 : "memory");
+}
+
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
+    uint32_t r[32];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+        "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]),
+          "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]),
+          "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]),
+          "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+        : "r"(taddr));
 #pragma unroll
-    for (int it = 0; it < kKeys * 16 / kThreads; ++it) {
-        const int idx = it * kThreads + threadIdx.x;
-        const int r = idx >> 4, ch = idx & 15;
-        const int key = k0 + r;
-        bool valid = key <= kend;
-        size_t off = 0;
-        if (valid) {
-            const int blk = table[key / BS];
-            if (blk < 0 || blk >= p.num_blocks) {
-                if (ch == 0) flag_error(p.d_err, PA_DEVERR_BLOCK_RANGE);
-                valid = false;
-            } else {
-                off = ((((size_t)blk * p.num_kv_heads + kvh) * BS + (key % BS)) * kD) * 2 + ch * 16;
-            }
-        }
-        const int so = swz(r, ch);
-        cp_async16(ks + so, kc + off, valid);
-        cp_async16(vs + so, vc + off, valid);
-    }
+    for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
 }
+
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const float (&v)[32]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+        "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
+        "r"(__float_as_uint(v[0])), "r"(__float_as_uint(v[1])), "r"(__float_as_uint(v[2])),
+        "r"(__float_as_uint(v[3])), "r"(__float_as_uint(v[4])), "r"(__float_as_uint(v[5])),
+        "r"(__float_as_uint(v[6])), "r"(__float_as_uint(v[7])), "r"(__float_as_uint(v[8])),
+        "r"(__float_as_uint(v[9])), "r"(__float_as_uint(v[10])), "r"(__float_as_uint(v[11])),
+        "r"(__float_as_uint(v[12])), "r"(__float_as_uint(v[13])), "r"(__float_as_uint(v[14])),
+        "r"(__float_as_uint(v[15])), "r"(__float_as_uint(v[16])), "r"(__float_as_uint(v[17])),
+        "r"(__float_as_uint(v[18])), "r"(__float_as_uint(v[19])), "r"(__float_as_uint(v[20])),
+        "r"(__float_as_uint(v[21])), "r"(__float_as_uint(v[22])), "r"(__float_as_uint(v[23])),
+        "r"(__float_as_uint(v[24])), "r"(__float_as_uint(v[25])), "r"(__float_as_uint(v[26])),
+        "r"(__float_as_uint(v[27])), "r"(__float_as_uint(v[28])), "r"(__float_as_uint(v[29])),
+        "r"(__float_as_uint(v[30])), "r"(__float_as_uint(v[31]))
+        : "memory");
+}
+
+__device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+__device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+
+__device__ __forceinline__ void tma_2d(uint32_t dst, const CUtensorMap *map, int x, int y, uint64_t *bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], "
+        "[%4];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_addr(bar))
+        : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive1(uint64_t *bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
+}
+
+__device__ __forceinline__ void wait_or_flag(uint64_t *bar, uint32_t parity, int *d_err) {
+    if (!mbar_wait(bar, parity)) flag_error(d_err, PA_DEVERR_TIMEOUT);
+}
+
+// ---- the kernel ------------------------------------------------------------
 
 template <typename T, int BS, int G>
-__global__ void __launch_bounds__(kThreads) prefill_kernel(const PrefillParams p) {
-    extern __shared__ __align__(128) unsigned char smem[];
+__global__ void __launch_bounds__(kThreads, 1)
+    prefill_tc_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap tmk,
+                      const __grid_constant__ CUtensorMap tmv) {
+    constexpr bool kBf16 = std::is_same<T, __nv_bfloat16>::value;
+    constexpr int kBlocksPerTile = kNK / BS;
+    static_assert(kNK % BS == 0 && kBlocksPerTile <= 32, "block_size");
+    static_assert(kM % G == 0, "group");
+
+    extern __shared__ unsigned char smem_raw[];
+    const uint32_t raw = smem_addr(smem_raw);
+    const uint32_t sb = (raw + 1023u) & ~1023u;  // 1 KB aligned: swizzle atoms start on 1 KB
+    unsigned char *gb = smem_raw + (sb - raw);
+    uint64_t *bars = reinterpret_cast<uint64_t *>(gb + kOffBar);
+    uint64_t *kv_full = bars + 0;   // [2] TMA -> MMA
+    uint64_t *kv_empty = bars + 2;  // [2] MMA -> TMA
+    uint64_t *q_full = bars + 4;    // softmax threads -> MMA (Q tile written)
+    uint64_t *s_full = bars + 5;    // [2] MMA -> softmax (S ready)
+    uint64_t *s_free = bars + 7;    // [2] softmax -> MMA (S read)
+    uint64_t *p_full = bars + 9;    // softmax -> MMA (P written, O rescaled)
+    uint64_t *pv_done = bars + 10;  // MMA -> softmax (PV finished)
+    volatile uint32_t *tmem_holder = reinterpret_cast<volatile uint32_t *>(bars + 12);
+
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int kvh = blockIdx.y;
-    const int row0 = blockIdx.x * kRows;  // first (position, head) row of this CTA
+    const int row0 = blockIdx.x * kM;
     const int nrows = p.chunk_len * G;
-    const int i_last = min(p.chunk_len - 1, (row0 + kRows - 1) / G);
+    const int i_last = min(p.chunk_len - 1, (row0 + kM - 1) / G);
     const int kend = p.prefix_len + i_last;  // last key any row of this CTA sees
-    const int ntiles = kend / kKeys + 1;
-    const int32_t *table = p.block_table;
+    const int ntiles = kend / kNK + 1;
 
-    const uint32_t sq = smem_addr(smem);
-    const uint32_t skv = sq + kQBytes;  // buffer b: K at skv + b*2*tile, V right after
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&kv_full[i], 1);
+            mbar_init(&kv_empty[i], 1);
+            mbar_init(&s_full[i], 1);
+            mbar_init(&s_free[i], 128);
+        }
+        mbar_init(q_full, 128);
+        mbar_init(p_full, 128);
+        mbar_init(pv_done, 1);
+        fence_barrier_init();
+    }
+    if (warp == 1) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                         smem_addr(const_cast<uint32_t *>(tmem_holder))),
+                     "r"(kTmemCols)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_holder;
+    const uint32_t tS0 = tmem, tO = tmem + 256;
 
-    // ---- Q tile: row r = (position i0 + r/G, head kvh*G + r%G), swizzled
-    {
-        const unsigned char *qg = static_cast<const unsigned char *>(p.query);
+    if (warp == 0) {
+        // ============================================================ producer
+        const int32_t *table = p.block_table;
+        const int oob_row = p.num_blocks * p.num_kv_heads * BS;  // first row past the pool: zero fill
+        for (int j = 0; j < ntiles; ++j) {
+            const int st = j & 1;
+            int y = oob_row;
+            if (lane < kBlocksPerTile) {
+                const int key0 = j * kNK + lane * BS;
+                if (key0 <= kend) {
+                    const int blk = table[key0 / BS];
+                    if (blk >= 0 && blk < p.num_blocks) y = (blk * p.num_kv_heads + kvh) * BS;
+                    else flag_error(p.d_err, PA_DEVERR_BLOCK_RANGE);
+                }
+            }
+            if (lane == 0) {
+                if (j >= 2) wait_or_flag(&kv_empty[st], (uint32_t)((j - 2) >> 1) & 1u, p.d_err);
+                mbar_arrive_expect_tx(&kv_full[st], 2u * kTileBytes);
+            }
+            __syncwarp();
+            if (lane < kBlocksPerTile) {
+                const uint32_t k_dst = sb + kOffKV + st * kStageBytes + lane * BS * 128;
+                const uint32_t v_dst = k_dst + kTileBytes;
+                tma_2d(k_dst, &tmk, 0, y, &kv_full[st]);
+                tma_2d(k_dst + kHalfBytes, &tmk, 64, y, &kv_full[st]);
+                tma_2d(v_dst, &tmv, 0, y, &kv_full[st]);
+                tma_2d(v_dst + kHalfBytes, &tmv, 64, y, &kv_full[st]);
+            }
+        }
+    } else if (warp == 1) {
+        // ============================================================ MMA issuer
+        if (lane == 0) {
+            constexpr uint32_t idesc_qk = instr_desc(kBf16, false);
+            constexpr uint32_t idesc_pv = instr_desc(kBf16, true);
+            const uint32_t q_s = sb + kOffQ, p_s = sb + kOffP;
+            auto issue_pv = [&](int jj) {
+                wait_or_flag(p_full, (uint32_t)jj & 1u, p.d_err);
+                tc_fence_after();
+                const uint32_t v_s = sb + kOffKV + (jj & 1) * kStageBytes + kTileBytes;
 #pragma unroll
-        for (int it = 0; it < kRows * 16 / kThreads; ++it) {
-            const int idx = it * kThreads + threadIdx.x;
-            const int r = idx >> 4, ch = idx & 15;
-            const int gr = row0 + r;
-            const bool valid = gr < nrows;
-            const int i = gr / G, h = gr % G;
-            const size_t off = valid ? ((((size_t)i * p.num_heads + kvh * G + h) * kD) * 2 + ch * 16) : 0;
-            cp_async16(sq + swz(r, ch), qg + off, valid);
+                for (int kk = 0; kk < 8; ++kk) {
+                    const uint64_t a = smem_desc(p_s + (kk >> 2) * kHalfBytes + (kk & 3) * 32, 16, 1024);
+                    const uint64_t b = smem_desc(v_s + kk * 2048, kHalfBytes, 1024);
+                    mma_f16(tO, a, b, idesc_pv, jj > 0 || kk > 0);
+                }
+                mma_commit(pv_done);
+                mma_commit(&kv_empty[jj & 1]);
+            };
+            wait_or_flag(q_full, 0, p.d_err);
+            tc_fence_after();
+            for (int j = 0; j < ntiles; ++j) {
+                const int st = j & 1;
+                wait_or_flag(&kv_full[st], (uint32_t)(j >> 1) & 1u, p.d_err);
+                if (j >= 2) wait_or_flag(&s_free[st], (uint32_t)((j - 2) >> 1) & 1u, p.d_err);
+                tc_fence_after();
+                const uint32_t k_s = sb + kOffKV + st * kStageBytes;
+#pragma unroll
+                for (int kk = 0; kk < 8; ++kk) {
+                    const uint32_t off = (kk >> 2) * kHalfBytes + (kk & 3) * 32;
+                    mma_f16(tS0 + st * 128, smem_desc(q_s + off, 16, 1024), smem_desc(k_s + off, 16, 1024),
+                            idesc_qk, kk > 0);
+                }
+                mma_commit(&s_full[st]);
+                if (j >= 1) issue_pv(j - 1);
+            }
+            issue_pv(ntiles - 1);
+        }
+    } else {
+        // ============================================================ softmax
+        const int quarter = warp & 3;
+        const int t = quarter * 32 + lane;  // query row of this thread = TMEM lane
+        const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
+        const int gr = row0 + t;
+        const bool valid = gr < nrows;
+        const int ipos = valid ? gr / G : 0, head = valid ? gr % G : 0;
+        const int plim = p.prefix_len + min(gr / G, p.chunk_len - 1);
+
+        // Q row t into the swizzled K-major tile
+        {
+            const uint4 *src = reinterpret_cast<const uint4 *>(static_cast<const T *>(p.query) +
+                                                               ((size_t)ipos * p.num_heads + kvh * G + head) * kD);
+#pragma unroll
+            for (int c = 0; c < 16; ++c) {
+                const uint4 v = valid ? src[c] : make_uint4(0, 0, 0, 0);
+                const uint32_t dst = sb + kOffQ + (c >> 3) * kHalfBytes + t * 128 + (((c & 7) ^ (t & 7)) << 4);
+                asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(dst), "r"(v.x), "r"(v.y), "r"(v.z),
+                             "r"(v.w)
+                             : "memory");
+            }
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            mbar_arrive1(q_full);
+        }
+
+        float m_run = -INFINITY, l_run = 0.f;
+        for (int j = 0; j < ntiles; ++j) {
+            const int st = j & 1;
+            wait_or_flag(&s_full[st], (uint32_t)(j >> 1) & 1u, p.d_err);
+            tc_fence_after();
+            float s[128];
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                float v[32];
+                tmem_ld32(tS0 + st * 128 + lane_off + c * 32, v);
+#pragma unroll
+                for (int e = 0; e < 32; ++e) s[c * 32 + e] = v[e];
+            }
+            tmem_wait_ld();
+            tc_fence_before();
+            mbar_arrive1(&s_free[st]);
+
+            const int kb = j * kNK;
+            float mx = -INFINITY;
+#pragma unroll
+            for (int c = 0; c < 128; ++c) {
+                const float v = (kb + c <= plim) ? s[c] * p.scale_log2 : -INFINITY;
+                s[c] = v;
+                mx = fmaxf(mx, v);
+            }
+            // PV of the previous tile must be done: it reads the P buffer and writes O
+            if (j >= 1) {
+                wait_or_flag(pv_done, (uint32_t)(j - 1) & 1u, p.d_err);
+                tc_fence_after();
+            }
+            if (mx > m_run + 8.0f) {
+                if (j >= 1 && m_run != -INFINITY) {
+                    const float alpha = fast_exp2(m_run - mx);
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) {
+                        float v[32];
+                        tmem_ld32(tO + lane_off + c * 32, v);
+                        tmem_wait_ld();
+#pragma unroll
+                        for (int e = 0; e < 32; ++e) v[e] *= alpha;
+                        tmem_st32(tO + lane_off + c * 32, v);
+                    }
+                    tmem_wait_st();
+                    l_run *= alpha;
+                }
+                m_run = mx;
+            }
+            // P row t, rounded to the input type, into the swizzled K-major tile
+#pragma unroll
+            for (int c = 0; c < 16; ++c) {
+                float pr[8];
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    pr[e] = fast_exp2(s[c * 8 + e] - m_run);
+                    l_run += pr[e];
+                }
+                const uint4 u = pack8<T>(pr);
+                const uint32_t dst = sb + kOffP + (c >> 3) * kHalfBytes + t * 128 + (((c & 7) ^ (t & 7)) << 4);
+                asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(dst), "r"(u.x), "r"(u.y), "r"(u.z),
+                             "r"(u.w)
+                             : "memory");
+            }
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            tc_fence_before();
+            mbar_arrive1(p_full);
+        }
+
+        // epilogue: O row / l, rounded once, stored
+        wait_or_flag(pv_done, (uint32_t)(ntiles - 1) & 1u, p.d_err);
+        tc_fence_after();
+        const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
+        T *orow = static_cast<T *>(p.out) + ((size_t)ipos * p.num_heads + kvh * G + head) * kD;
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+            float v[32];
+            tmem_ld32(tO + lane_off + c * 32, v);
+            tmem_wait_ld();
+            if (valid) {
+#pragma unroll
+                for (int q8 = 0; q8 < 4; ++q8) {
+                    float o8[8];
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) o8[e] = v[q8 * 8 + e] * inv;
+                    *reinterpret_cast<uint4 *>(orow + c * 32 + q8 * 8) = pack8<T>(o8);
+                }
+            }
         }
     }
-    load_kv_tile<BS>(p, skv, skv + kTileBytes, 0, kend, kvh, table);
-    cp_async_commit();
 
-    // per-thread rows: g and g+8 of the warp's 16
-    const int g = lane >> 2, t4 = lane & 3;
-    const int wrow = warp * 16;
-    int pos_lim[2];  // last key each of the thread's two rows may see
-#pragma unroll
-    for (int hr = 0; hr < 2; ++hr) {
-        const int gr = row0 + wrow + g + 8 * hr;
-        pos_lim[hr] = p.prefix_len + min(gr / G, p.chunk_len - 1);
-    }
-
-    float o[16][4];  // O[16 rows][128 dims]: 16 n-tiles of 8 dims
-#pragma unroll
-    for (int n = 0; n < 16; ++n)
-#pragma unroll
-        for (int e = 0; e < 4; ++e) o[n][e] = 0.f;
-    float m_run[2] = {-INFINITY, -INFINITY};
-    float l_run[2] = {0.f, 0.f};
-    uint32_t qa[8][4];  // Q fragments for the 8 k-steps of 16 dims
-
-    for (int tile = 0; tile < ntiles; ++tile) {
-        const int buf = tile & 1;
-        const uint32_t ks = skv + buf * 2 * kTileBytes;
-        const uint32_t vs = ks + kTileBytes;
-        if (tile + 1 < ntiles) {
-            const uint32_t nks = skv + (buf ^ 1) * 2 * kTileBytes;
-            load_kv_tile<BS>(p, nks, nks + kTileBytes, (tile + 1) * kKeys, kend, kvh, table);
-            cp_async_commit();
-            cp_async_wait<1>();
-        } else {
-            cp_async_wait<0>();
-        }
-        __syncthreads();
-        if (tile == 0) {
-            // Q fragments: lane l supplies row l%16, column block 8*(l/16) of each 16x16 block
-#pragma unroll
-            for (int kk = 0; kk < 8; ++kk)
-                ldsm_x4(sq + swz(wrow + (lane & 15), kk * 2 + (lane >> 4)), qa[kk]);
-        }
-
-        // ---- S = Q K^T for 64 keys: 8 n-tiles of 8 keys
-        float s[8][4];
-#pragma unroll
-        for (int n = 0; n < 8; ++n)
-#pragma unroll
-            for (int e = 0; e < 4; ++e) s[n][e] = 0.f;
-#pragma unroll
-        for (int kk = 0; kk < 8; ++kk) {
-#pragma unroll
-            for (int n2 = 0; n2 < 4; ++n2) {  // two n-tiles (16 keys) per ldmatrix.x4
-                uint32_t b[4];
-                const int key = n2 * 16 + (lane & 7) + ((lane >> 4) << 3);
-                const int ch = kk * 2 + ((lane >> 3) & 1);
-                ldsm_x4(ks + swz(key, ch), b);
-                Mma<T>::run(s[2 * n2], qa[kk], b[0], b[1]);
-                Mma<T>::run(s[2 * n2 + 1], qa[kk], b[2], b[3]);
-            }
-        }
-
-        // ---- causal mask, online softmax (log2 units)
-        const int kbase = tile * kKeys;
-        float mt[2] = {-INFINITY, -INFINITY};
-#pragma unroll
-        for (int n = 0; n < 8; ++n)
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const int hr = e >> 1;
-                const int key = kbase + n * 8 + 2 * t4 + (e & 1);
-                float v = s[n][e] * p.scale_log2;
-                v = key <= pos_lim[hr] ? v : -INFINITY;
-                s[n][e] = v;
-                mt[hr] = fmaxf(mt[hr], v);
-            }
-        float alpha[2];
-#pragma unroll
-        for (int hr = 0; hr < 2; ++hr) {
-            mt[hr] = fmaxf(mt[hr], __shfl_xor_sync(kFull, mt[hr], 1));
-            mt[hr] = fmaxf(mt[hr], __shfl_xor_sync(kFull, mt[hr], 2));
-            const float mn = fmaxf(m_run[hr], mt[hr]);
-            alpha[hr] = m_run[hr] == -INFINITY ? 0.f : fast_exp2(m_run[hr] - mn);
-            m_run[hr] = mn;
-            l_run[hr] *= alpha[hr];
-        }
-#pragma unroll
-        for (int n = 0; n < 16; ++n) {
-            o[n][0] *= alpha[0];
-            o[n][1] *= alpha[0];
-            o[n][2] *= alpha[1];
-            o[n][3] *= alpha[1];
-        }
-        uint32_t pa_[4][4];  // P as A fragments for the 4 k-steps of 16 keys
-#pragma unroll
-        for (int n = 0; n < 8; ++n) {
-            const float p0 = m_run[0] == -INFINITY ? 0.f : fast_exp2(s[n][0] - m_run[0]);
-            const float p1 = m_run[0] == -INFINITY ? 0.f : fast_exp2(s[n][1] - m_run[0]);
-            const float p2 = m_run[1] == -INFINITY ? 0.f : fast_exp2(s[n][2] - m_run[1]);
-            const float p3 = m_run[1] == -INFINITY ? 0.f : fast_exp2(s[n][3] - m_run[1]);
-            l_run[0] += p0 + p1;
-            l_run[1] += p2 + p3;
-            const int kk = n >> 1, hi = n & 1;
-            pa_[kk][2 * hi] = Elem<T>::pack2(p0, p1);
-            pa_[kk][2 * hi + 1] = Elem<T>::pack2(p2, p3);
-        }
-
-        // ---- O += P V: 4 k-steps of 16 keys, 16 n-tiles of 8 dims
-#pragma unroll
-        for (int kk = 0; kk < 4; ++kk) {
-#pragma unroll
-            for (int n2 = 0; n2 < 8; ++n2) {  // two dim n-tiles per ldmatrix.x4.trans
-                uint32_t b[4];
-                const int key = kk * 16 + (lane & 7) + (((lane >> 3) & 1) << 3);
-                const int ch = n2 * 2 + (lane >> 4);
-                ldsm_x4_t(vs + swz(key, ch), b);
-                Mma<T>::run(o[2 * n2], pa_[kk], b[0], b[1]);
-                Mma<T>::run(o[2 * n2 + 1], pa_[kk], b[2], b[3]);
-            }
-        }
-        __syncthreads();  // this buffer is refilled in the next iteration
-    }
-
-    // ---- normalise and store rows (position, head)
-#pragma unroll
-    for (int hr = 0; hr < 2; ++hr) {
-        float l = l_run[hr];
-        l += __shfl_xor_sync(kFull, l, 1);
-        l += __shfl_xor_sync(kFull, l, 2);
-        const float inv = l > 0.f ? 1.f / l : 0.f;
-        const int gr = row0 + wrow + g + 8 * hr;
-        if (gr < nrows) {
-            const int i = gr / G, h = gr % G;
-            T *orow = static_cast<T *>(p.out) + ((size_t)i * p.num_heads + kvh * G + h) * kD;
-#pragma unroll
-            for (int n = 0; n < 16; ++n) {
-                const uint32_t v = Elem<T>::pack2(o[n][2 * hr] * inv, o[n][2 * hr + 1] * inv);
-                *reinterpret_cast<uint32_t *>(orow + n * 8 + 2 * t4) = v;
-            }
-        }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols)
+                     : "memory");
     }
 }
 
+// ---- host side -------------------------------------------------------------
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
+                                   const cuuint64_t *, const cuuint32_t *, const cuuint32_t *,
+                                   CUtensorMapInterleave, CUtensorMapSwizzle, CUtensorMapL2promotion,
+                                   CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+    static EncodeTiledFn fn = nullptr;
+    if (!fn) {
+        void *ptr = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) !=
+                cudaSuccess ||
+            q != cudaDriverEntryPointSuccess)
+            return nullptr;
+        fn = reinterpret_cast<EncodeTiledFn>(ptr);
+    }
+    return fn;
+}
+
+// The pool as a 2-D tensor [num_blocks*num_kv_heads*block_size rows][128]; a
+// box is 64 elements (128 bytes) by block_size rows, 128-byte swizzled.
+bool make_pool_map(CUtensorMap *map, const void *pool, const PrefillParams &p, int bs, bool bf16) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return false;
+    const cuuint64_t dims[2] = {(cuuint64_t)kD, (cuuint64_t)p.num_blocks * p.num_kv_heads * bs};
+    const cuuint64_t strides[1] = {(cuuint64_t)kD * 2};
+    const cuuint32_t box[2] = {64, (cuuint32_t)bs};
+    const cuuint32_t estr[2] = {1, 1};
+    return fn(map, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2,
+              const_cast<void *>(pool), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+              CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 template <typename T, int BS, int G>
-int launch_prefill_t(const PrefillParams &p, cudaStream_t stream) {
-    auto kern = prefill_kernel<T, BS, G>;
+int launch_tc_t(const PrefillParams &p, cudaStream_t stream) {
+    auto kern = prefill_tc_kernel<T, BS, G>;
     static bool attr_set = false;
     if (!attr_set) {
-        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem) != cudaSuccess)
+        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemAlloc) != cudaSuccess)
             return PA_ERR_CUDA;
         attr_set = true;
     }
-    const int rows = p.chunk_len * G;
-    dim3 grid((rows + kRows - 1) / kRows, p.num_kv_heads);
-    kern<<<grid, kThreads, kSmem, stream>>>(p);
+    const bool bf16 = std::is_same<T, __nv_bfloat16>::value;
+    CUtensorMap tmk, tmv;
+    if (!make_pool_map(&tmk, p.k_cache, p, BS, bf16) || !make_pool_map(&tmv, p.v_cache, p, BS, bf16))
+        return PA_ERR_CUDA;
+    dim3 grid((p.chunk_len * G + kM - 1) / kM, p.num_kv_heads);
+    kern<<<grid, kThreads, kSmemAlloc, stream>>>(p, tmk, tmv);
     return cudaPeekAtLastError() == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }
 
 template <typename T>
-int launch_prefill_dtype(int block_size, int group, const PrefillParams &p, cudaStream_t stream) {
-#define PA_PREFILL_CASE(BB, GG) \
-    if (block_size == BB && group == GG) return launch_prefill_t<T, BB, GG>(p, stream);
-#define PA_PREFILL_GROUPS(BB) \
-    PA_PREFILL_CASE(BB, 1) PA_PREFILL_CASE(BB, 2) PA_PREFILL_CASE(BB, 4) PA_PREFILL_CASE(BB, 8)
-    PA_PREFILL_GROUPS(16)
-    PA_PREFILL_GROUPS(32)
-#undef PA_PREFILL_GROUPS
-#undef PA_PREFILL_CASE
+int launch_tc_dtype(int block_size, int group, const PrefillParams &p, cudaStream_t stream) {
+#define PA_TC_CASE(BB, GG) \
+    if (block_size == BB && group == GG) return launch_tc_t<T, BB, GG>(p, stream);
+#define PA_TC_GROUPS(BB) PA_TC_CASE(BB, 1) PA_TC_CASE(BB, 2) PA_TC_CASE(BB, 4) PA_TC_CASE(BB, 8)
+    PA_TC_GROUPS(16)
+    PA_TC_GROUPS(32)
+#undef PA_TC_GROUPS
+#undef PA_TC_CASE
     return PA_ERR_UNSUPPORTED;
 }
 
@@ -317,8 +454,10 @@ int launch_prefill_dtype(int block_size, int group, const PrefillParams &p, cuda
 int launch_prefill(pa_dtype dt, int head_dim, int block_size, int group, const PrefillParams &p,
                    cudaStream_t stream) {
     if (head_dim != kD) return PA_ERR_UNSUPPORTED;
-    return dt == PA_BF16 ? launch_prefill_dtype<__nv_bfloat16>(block_size, group, p, stream)
-                         : launch_prefill_dtype<__half>(block_size, group, p, stream);
+    // TMA row coordinates are 32-bit
+    if ((long long)p.num_blocks * p.num_kv_heads * block_size >= (1LL << 31)) return PA_ERR_UNSUPPORTED;
+    return dt == PA_BF16 ? launch_tc_dtype<__nv_bfloat16>(block_size, group, p, stream)
+                         : launch_tc_dtype<__half>(block_size, group, p, stream);
 }
 
 }  // namespace pa
