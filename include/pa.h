@@ -203,6 +203,7 @@ PA_API int pa_copy_blocks(void *k_cache, void *v_cache, const int64_t *pairs, in
  *   out    [chunk_len][num_heads][head_dim] dtype (written)
  *   query  [chunk_len][num_heads][head_dim] dtype
  *   block_table int32 [>= ceil((prefix_len+chunk_len)/block_size)]
+ * scale must be finite and > 0.
  * Supported: head_dim 128, block_size in {16, 32}, group size in {1,2,4,8},
  * dtype f16 or bf16.
  */

@@ -189,7 +189,7 @@ int pa_prefill_chunk(void *out, const void *query, const void *k_cache, const vo
         block_size <= 0 || num_blocks <= 0 || !good_dtype(dtype))
         return PA_ERR_INVALID_ARG;
     if (num_heads % num_kv_heads) return PA_ERR_INVALID_ARG;
-    if (!std::isfinite(scale)) return PA_ERR_OUT_OF_RANGE;
+    if (!std::isfinite(scale) || !(scale > 0.f)) return PA_ERR_OUT_OF_RANGE;
     if (chunk_len == 0) return PA_OK;
     if (!out || !query || !k_cache || !v_cache || !block_table) return PA_ERR_INVALID_ARG;
     if (!aligned16(out) || !aligned16(query) || !aligned16(k_cache) || !aligned16(v_cache))

@@ -16,8 +16,10 @@
 //   warps 2-5 softmax: each thread owns one query row = one TMEM lane; reads
 //             its S row, applies the causal mask, updates the running max
 //             (rescaling O in TMEM only when the max grows by more than 2^8),
-//             writes P (rounded to the input type) into shared memory for the
-//             PV MMA, and finally normalises O and stores the row.
+//             writes P (rounded to the input type) into one of two shared
+//             buffers for the PV MMA, and finally normalises O and stores the
+//             row.  With two P buffers the softmax of tile j overlaps PV of
+//             tile j-1; it waits for that PV only when O must be rescaled.
 // All waits are bounded; a wait that gives up flags PA_DEVERR_TIMEOUT.
 #include <cuda.h>
 
@@ -38,7 +40,7 @@ constexpr int kOffQ = 0;
 constexpr int kOffKV = kOffQ + kTileBytes;                 // stage s: K at +64 KB*s, V after it
 constexpr int kStageBytes = 2 * kTileBytes;
 constexpr int kOffP = kOffKV + 2 * kStageBytes;            // 160 KB
-constexpr int kOffBar = kOffP + kTileBytes;                // 192 KB
+constexpr int kOffBar = kOffP + 2 * kTileBytes;            // 224 KB (P double-buffered)
 constexpr int kSmemUsed = kOffBar + 128;
 constexpr int kSmemAlloc = kSmemUsed + 1024;               // room to align the base to 1 KB
 constexpr int kThreads = 192;
@@ -155,9 +157,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint64_t *q_full = bars + 4;    // softmax threads -> MMA (Q tile written)
     uint64_t *s_full = bars + 5;    // [2] MMA -> softmax (S ready)
     uint64_t *s_free = bars + 7;    // [2] softmax -> MMA (S read)
-    uint64_t *p_full = bars + 9;    // softmax -> MMA (P written, O rescaled)
-    uint64_t *pv_done = bars + 10;  // MMA -> softmax (PV finished)
-    volatile uint32_t *tmem_holder = reinterpret_cast<volatile uint32_t *>(bars + 12);
+    uint64_t *p_full = bars + 9;    // [2] softmax -> MMA (P buffer written, O rescaled)
+    uint64_t *pv_done = bars + 11;  // [2] MMA -> softmax (PV of that P buffer finished)
+    volatile uint32_t *tmem_holder = reinterpret_cast<volatile uint32_t *>(bars + 13);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int kvh = blockIdx.y;
@@ -173,10 +175,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(&kv_empty[i], 1);
             mbar_init(&s_full[i], 1);
             mbar_init(&s_free[i], 128);
+            mbar_init(&p_full[i], 128);
+            mbar_init(&pv_done[i], 1);
         }
         mbar_init(q_full, 128);
-        mbar_init(p_full, 128);
-        mbar_init(pv_done, 1);
         fence_barrier_init();
     }
     if (warp == 1) {
@@ -196,16 +198,20 @@ __global__ void __launch_bounds__(kThreads, 1)
         // ============================================================ producer
         const int32_t *table = p.block_table;
         const int oob_row = p.num_blocks * p.num_kv_heads * BS;  // first row past the pool: zero fill
+        // lane b < kBlocksPerTile handles block b of each tile; entries load one tile ahead
+        auto entry = [&](int jt) {
+            const int key0 = jt * kNK + lane * BS;
+            return (lane < kBlocksPerTile && key0 <= kend) ? table[key0 / BS] : -1;
+        };
+        int blk_next = entry(0);
         for (int j = 0; j < ntiles; ++j) {
             const int st = j & 1;
+            const int blk = blk_next;
+            if (j + 1 < ntiles) blk_next = entry(j + 1);
             int y = oob_row;
-            if (lane < kBlocksPerTile) {
-                const int key0 = j * kNK + lane * BS;
-                if (key0 <= kend) {
-                    const int blk = table[key0 / BS];
-                    if (blk >= 0 && blk < p.num_blocks) y = (blk * p.num_kv_heads + kvh) * BS;
-                    else flag_error(p.d_err, PA_DEVERR_BLOCK_RANGE);
-                }
+            if (lane < kBlocksPerTile && j * kNK + lane * BS <= kend) {
+                if (blk >= 0 && blk < p.num_blocks) y = (blk * p.num_kv_heads + kvh) * BS;
+                else flag_error(p.d_err, PA_DEVERR_BLOCK_RANGE);
             }
             if (lane == 0) {
                 if (j >= 2) wait_or_flag(&kv_empty[st], (uint32_t)((j - 2) >> 1) & 1u, p.d_err);
@@ -226,10 +232,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) {
             constexpr uint32_t idesc_qk = instr_desc(kBf16, false);
             constexpr uint32_t idesc_pv = instr_desc(kBf16, true);
-            const uint32_t q_s = sb + kOffQ, p_s = sb + kOffP;
+            const uint32_t q_s = sb + kOffQ;
             auto issue_pv = [&](int jj) {
-                wait_or_flag(p_full, (uint32_t)jj & 1u, p.d_err);
+                const int pb = jj & 1;
+                wait_or_flag(&p_full[pb], (uint32_t)(jj >> 1) & 1u, p.d_err);
                 tc_fence_after();
+                const uint32_t p_s = sb + kOffP + pb * kTileBytes;
                 const uint32_t v_s = sb + kOffKV + (jj & 1) * kStageBytes + kTileBytes;
 #pragma unroll
                 for (int kk = 0; kk < 8; ++kk) {
@@ -237,7 +245,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const uint64_t b = smem_desc(v_s + kk * 2048, kHalfBytes, 1024);
                     mma_f16(tO, a, b, idesc_pv, jj > 0 || kk > 0);
                 }
-                mma_commit(pv_done);
+                mma_commit(&pv_done[pb]);
                 mma_commit(&kv_empty[jj & 1]);
             };
             wait_or_flag(q_full, 0, p.d_err);
@@ -268,6 +276,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         const bool valid = gr < nrows;
         const int ipos = valid ? gr / G : 0, head = valid ? gr % G : 0;
         const int plim = p.prefix_len + min(gr / G, p.chunk_len - 1);
+        const int plim_cta = p.prefix_len + row0 / G;  // smallest limit of any row in the CTA
+        const float csc = p.scale_log2;                 // > 0 (checked on the host)
 
         // Q row t into the swizzled K-major tile
         {
@@ -285,7 +295,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_arrive1(q_full);
         }
 
-        float m_run = -INFINITY, l_run = 0.f;
+        float m_run = -INFINITY;  // running max in scaled log2 units
+        float l8[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) l8[e] = 0.f;
         for (int j = 0; j < ntiles; ++j) {
             const int st = j & 1;
             wait_or_flag(&s_full[st], (uint32_t)(j >> 1) & 1u, p.d_err);
@@ -302,21 +315,32 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_fence_before();
             mbar_arrive1(&s_free[st]);
 
+            // causal mask only on tiles that reach past some row's limit
             const int kb = j * kNK;
-            float mx = -INFINITY;
+            if (kb + kNK - 1 > plim_cta) {
 #pragma unroll
-            for (int c = 0; c < 128; ++c) {
-                const float v = (kb + c <= plim) ? s[c] * p.scale_log2 : -INFINITY;
-                s[c] = v;
-                mx = fmaxf(mx, v);
+                for (int c = 0; c < 128; ++c) s[c] = (kb + c <= plim) ? s[c] : -INFINITY;
             }
-            // PV of the previous tile must be done: it reads the P buffer and writes O
-            if (j >= 1) {
-                wait_or_flag(pv_done, (uint32_t)(j - 1) & 1u, p.d_err);
+            float mx8[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) mx8[e] = s[e];
+#pragma unroll
+            for (int c = 8; c < 128; ++c) mx8[c & 7] = fmaxf(mx8[c & 7], s[c]);
+            float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
+                             fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
+            mx *= csc;
+
+            // the P buffer of this tile was last read by PV of tile j-2
+            const int pb = j & 1;
+            if (j >= 2) {
+                wait_or_flag(&pv_done[pb], (uint32_t)((j - 2) >> 1) & 1u, p.d_err);
                 tc_fence_after();
             }
             if (mx > m_run + 8.0f) {
                 if (j >= 1 && m_run != -INFINITY) {
+                    // O must hold every PV so far before it is rescaled
+                    wait_or_flag(&pv_done[(j - 1) & 1], (uint32_t)((j - 1) >> 1) & 1u, p.d_err);
+                    tc_fence_after();
                     const float alpha = fast_exp2(m_run - mx);
 #pragma unroll
                     for (int c = 0; c < 4; ++c) {
@@ -328,33 +352,37 @@ __global__ void __launch_bounds__(kThreads, 1)
                         tmem_st32(tO + lane_off + c * 32, v);
                     }
                     tmem_wait_st();
-                    l_run *= alpha;
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) l8[e] *= alpha;
                 }
                 m_run = mx;
             }
-            // P row t, rounded to the input type, into the swizzled K-major tile
+            // P row t = 2^(s*scale - max), rounded to the input type, swizzled K-major
+            const float neg_m = -m_run;
+            const uint32_t pbase = sb + kOffP + pb * kTileBytes;
 #pragma unroll
             for (int c = 0; c < 16; ++c) {
                 float pr[8];
 #pragma unroll
                 for (int e = 0; e < 8; ++e) {
-                    pr[e] = fast_exp2(s[c * 8 + e] - m_run);
-                    l_run += pr[e];
+                    pr[e] = fast_exp2(fmaf(s[c * 8 + e], csc, neg_m));
+                    l8[e] += pr[e];
                 }
                 const uint4 u = pack8<T>(pr);
-                const uint32_t dst = sb + kOffP + (c >> 3) * kHalfBytes + t * 128 + (((c & 7) ^ (t & 7)) << 4);
+                const uint32_t dst = pbase + (c >> 3) * kHalfBytes + t * 128 + (((c & 7) ^ (t & 7)) << 4);
                 asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(dst), "r"(u.x), "r"(u.y), "r"(u.z),
                              "r"(u.w)
                              : "memory");
             }
             asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
             tc_fence_before();
-            mbar_arrive1(p_full);
+            mbar_arrive1(&p_full[pb]);
         }
 
         // epilogue: O row / l, rounded once, stored
-        wait_or_flag(pv_done, (uint32_t)(ntiles - 1) & 1u, p.d_err);
+        wait_or_flag(&pv_done[(ntiles - 1) & 1], (uint32_t)((ntiles - 1) >> 1) & 1u, p.d_err);
         tc_fence_after();
+        const float l_run = ((l8[0] + l8[1]) + (l8[2] + l8[3])) + ((l8[4] + l8[5]) + (l8[6] + l8[7]));
         const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
         T *orow = static_cast<T *>(p.out) + ((size_t)ipos * p.num_heads + kvh * G + head) * kD;
 #pragma unroll
