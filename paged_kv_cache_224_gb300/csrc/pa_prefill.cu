@@ -7,10 +7,10 @@
 // block table.
 //
 // One CTA computes 128 query rows -- 128/G chunk positions times the G query
-// heads of one kv head -- against 128-key tiles:
+// heads of one kv head -- against 64-key tiles:
 //   warp 0    TMA producer: for each key tile, one 2-D tensor copy per
 //             (block, 64-dim half) of K and of V, straight from the paged pool
-//             into a 128-byte-swizzled shared layout (two stages);
+//             into a 128-byte-swizzled shared layout (four stages in flight);
 //   warp 1    MMA issuer (one thread): S = Q K^T into TMEM (two buffers), then
 //             O += P V into TMEM, tcgen05.mma kind::f16, fp32 accumulation;
 //   warps 2-5 softmax: each thread owns one query row = one TMEM lane; reads
@@ -20,6 +20,8 @@
 //             buffers for the PV MMA, and finally normalises O and stores the
 //             row.  With two P buffers the softmax of tile j overlaps PV of
 //             tile j-1; it waits for that PV only when O must be rescaled.
+//             On the last tile it zeroes the V rows past the CTA's last key,
+//             so garbage (even NaN) in unused slots never reaches O.
 // All waits are bounded; a wait that gives up flags PA_DEVERR_TIMEOUT.
 #include <cuda.h>
 
@@ -31,20 +33,24 @@
 namespace pa {
 namespace {
 
-constexpr int kD = 128;                     // head_dim
-constexpr int kM = 128;                     // query rows per CTA
-constexpr int kNK = 128;                    // keys per tile
-constexpr int kHalfBytes = 128 * 128;       // 128 rows x 64 elements x 2 bytes
-constexpr int kTileBytes = 2 * kHalfBytes;  // 32 KB: one operand tile (two 64-dim halves)
+constexpr int kD = 128;                        // head_dim
+constexpr int kM = 128;                        // query rows per CTA
+constexpr int kNK = 64;                        // keys per tile
+constexpr int kStages = 4;                     // K/V tiles in flight
+constexpr int kQHalf = kM * 128;               // one 64-dim half of Q: 128 rows x 128 bytes
+constexpr int kKVHalf = kNK * 128;             // one 64-dim half of a K or V tile
+constexpr int kKVTile = 2 * kKVHalf;           // 16 KB
+constexpr int kStageBytes = 2 * kKVTile;       // K tile + V tile
+constexpr int kPBytes = kM * kNK * 2;          // P: 128 rows x 64 keys = one 128-byte-wide half
 constexpr int kOffQ = 0;
-constexpr int kOffKV = kOffQ + kTileBytes;                 // stage s: K at +64 KB*s, V after it
-constexpr int kStageBytes = 2 * kTileBytes;
-constexpr int kOffP = kOffKV + 2 * kStageBytes;            // 160 KB
-constexpr int kOffBar = kOffP + 2 * kTileBytes;            // 224 KB (P double-buffered)
-constexpr int kSmemUsed = kOffBar + 128;
+constexpr int kOffKV = kOffQ + 2 * kQHalf;                 // 32 KB
+constexpr int kOffP = kOffKV + kStages * kStageBytes;      // 160 KB, two P buffers
+constexpr int kOffBar = kOffP + 2 * kPBytes;               // 192 KB
+constexpr int kSmemUsed = kOffBar + 256;
 constexpr int kSmemAlloc = kSmemUsed + 1024;               // room to align the base to 1 KB
 constexpr int kThreads = 192;
-constexpr uint32_t kTmemCols = 512;                        // S0, S1, O (128 columns each)
+constexpr uint32_t kTmemCols = 256;                        // S0, S1 (64 columns each), O (128)
+static_assert(kNK * 2 == 128, "P rows are one 128-byte swizzle row");
 
 // ---- tcgen05 / TMA wrappers (inline PTX) ---------------------------------
 
@@ -63,10 +69,10 @@ __device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint32_t lbo, uint
 }
 
 // Instruction descriptor, kind::f16: fp32 accumulator, A and B both fp16 or
-// both bf16, A K-major, B K-major or MN-major, M = N = 128.
-__host__ __device__ constexpr uint32_t instr_desc(bool bf16, bool b_mn_major) {
+// both bf16, A K-major, B K-major or MN-major, M = 128, N given.
+__host__ __device__ constexpr uint32_t instr_desc(bool bf16, bool b_mn_major, int n) {
     return (1u << 4) | ((bf16 ? 1u : 0u) << 7) | ((bf16 ? 1u : 0u) << 10) |
-           ((b_mn_major ? 1u : 0u) << 16) | ((uint32_t)(128 >> 3) << 17) | ((uint32_t)(128 >> 4) << 24);
+           ((b_mn_major ? 1u : 0u) << 16) | ((uint32_t)(n >> 3) << 17) | ((uint32_t)(128 >> 4) << 24);
 }
 
 __device__ __forceinline__ void mma_f16(uint32_t tmem_d, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
@@ -152,14 +158,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t sb = (raw + 1023u) & ~1023u;  // 1 KB aligned: swizzle atoms start on 1 KB
     unsigned char *gb = smem_raw + (sb - raw);
     uint64_t *bars = reinterpret_cast<uint64_t *>(gb + kOffBar);
-    uint64_t *kv_full = bars + 0;   // [2] TMA -> MMA
-    uint64_t *kv_empty = bars + 2;  // [2] MMA -> TMA
-    uint64_t *q_full = bars + 4;    // softmax threads -> MMA (Q tile written)
-    uint64_t *s_full = bars + 5;    // [2] MMA -> softmax (S ready)
-    uint64_t *s_free = bars + 7;    // [2] softmax -> MMA (S read)
-    uint64_t *p_full = bars + 9;    // [2] softmax -> MMA (P buffer written, O rescaled)
-    uint64_t *pv_done = bars + 11;  // [2] MMA -> softmax (PV of that P buffer finished)
-    volatile uint32_t *tmem_holder = reinterpret_cast<volatile uint32_t *>(bars + 13);
+    uint64_t *kv_full = bars + 0;   // [kStages] TMA -> MMA
+    uint64_t *kv_empty = bars + 4;  // [kStages] MMA -> TMA
+    uint64_t *q_full = bars + 8;    // softmax threads -> MMA (Q tile written)
+    uint64_t *s_full = bars + 9;    // [2] MMA -> softmax (S ready)
+    uint64_t *s_free = bars + 11;   // [2] softmax -> MMA (S read)
+    uint64_t *p_full = bars + 13;   // [2] softmax -> MMA (P buffer written, O rescaled)
+    uint64_t *pv_done = bars + 15;  // [2] MMA -> softmax (PV of that P buffer finished)
+    volatile uint32_t *tmem_holder = reinterpret_cast<volatile uint32_t *>(bars + 17);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int kvh = blockIdx.y;
@@ -170,9 +176,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int ntiles = kend / kNK + 1;
 
     if (threadIdx.x == 0) {
-        for (int i = 0; i < 2; ++i) {
+        for (int i = 0; i < kStages; ++i) {
             mbar_init(&kv_full[i], 1);
             mbar_init(&kv_empty[i], 1);
+        }
+        for (int i = 0; i < 2; ++i) {
             mbar_init(&s_full[i], 1);
             mbar_init(&s_free[i], 128);
             mbar_init(&p_full[i], 128);
@@ -192,7 +200,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_holder;
-    const uint32_t tS0 = tmem, tO = tmem + 256;
+    const uint32_t tS0 = tmem, tO = tmem + 2 * kNK;
 
     if (warp == 0) {
         // ============================================================ producer
@@ -205,7 +213,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         };
         int blk_next = entry(0);
         for (int j = 0; j < ntiles; ++j) {
-            const int st = j & 1;
+            const int st = j % kStages;
             const int blk = blk_next;
             if (j + 1 < ntiles) blk_next = entry(j + 1);
             int y = oob_row;
@@ -214,55 +222,56 @@ __global__ void __launch_bounds__(kThreads, 1)
                 else flag_error(p.d_err, PA_DEVERR_BLOCK_RANGE);
             }
             if (lane == 0) {
-                if (j >= 2) wait_or_flag(&kv_empty[st], (uint32_t)((j - 2) >> 1) & 1u, p.d_err);
-                mbar_arrive_expect_tx(&kv_full[st], 2u * kTileBytes);
+                if (j >= kStages) wait_or_flag(&kv_empty[st], (uint32_t)(j / kStages - 1) & 1u, p.d_err);
+                mbar_arrive_expect_tx(&kv_full[st], 2u * kKVTile);
             }
             __syncwarp();
             if (lane < kBlocksPerTile) {
                 const uint32_t k_dst = sb + kOffKV + st * kStageBytes + lane * BS * 128;
-                const uint32_t v_dst = k_dst + kTileBytes;
+                const uint32_t v_dst = k_dst + kKVTile;
                 tma_2d(k_dst, &tmk, 0, y, &kv_full[st]);
-                tma_2d(k_dst + kHalfBytes, &tmk, 64, y, &kv_full[st]);
+                tma_2d(k_dst + kKVHalf, &tmk, 64, y, &kv_full[st]);
                 tma_2d(v_dst, &tmv, 0, y, &kv_full[st]);
-                tma_2d(v_dst + kHalfBytes, &tmv, 64, y, &kv_full[st]);
+                tma_2d(v_dst + kKVHalf, &tmv, 64, y, &kv_full[st]);
             }
         }
     } else if (warp == 1) {
         // ============================================================ MMA issuer
         if (lane == 0) {
-            constexpr uint32_t idesc_qk = instr_desc(kBf16, false);
-            constexpr uint32_t idesc_pv = instr_desc(kBf16, true);
+            constexpr uint32_t idesc_qk = instr_desc(kBf16, false, kNK);
+            constexpr uint32_t idesc_pv = instr_desc(kBf16, true, kD);
             const uint32_t q_s = sb + kOffQ;
             auto issue_pv = [&](int jj) {
                 const int pb = jj & 1;
+                const int stage = jj % kStages;
                 wait_or_flag(&p_full[pb], (uint32_t)(jj >> 1) & 1u, p.d_err);
                 tc_fence_after();
-                const uint32_t p_s = sb + kOffP + pb * kTileBytes;
-                const uint32_t v_s = sb + kOffKV + (jj & 1) * kStageBytes + kTileBytes;
+                const uint32_t p_s = sb + kOffP + pb * kPBytes;
+                const uint32_t v_s = sb + kOffKV + stage * kStageBytes + kKVTile;
 #pragma unroll
-                for (int kk = 0; kk < 8; ++kk) {
-                    const uint64_t a = smem_desc(p_s + (kk >> 2) * kHalfBytes + (kk & 3) * 32, 16, 1024);
-                    const uint64_t b = smem_desc(v_s + kk * 2048, kHalfBytes, 1024);
+                for (int kk = 0; kk < kNK / 16; ++kk) {
+                    const uint64_t a = smem_desc(p_s + kk * 32, 16, 1024);
+                    const uint64_t b = smem_desc(v_s + kk * 2048, kKVHalf, 1024);
                     mma_f16(tO, a, b, idesc_pv, jj > 0 || kk > 0);
                 }
                 mma_commit(&pv_done[pb]);
-                mma_commit(&kv_empty[jj & 1]);
+                mma_commit(&kv_empty[stage]);
             };
             wait_or_flag(q_full, 0, p.d_err);
             tc_fence_after();
             for (int j = 0; j < ntiles; ++j) {
-                const int st = j & 1;
-                wait_or_flag(&kv_full[st], (uint32_t)(j >> 1) & 1u, p.d_err);
-                if (j >= 2) wait_or_flag(&s_free[st], (uint32_t)((j - 2) >> 1) & 1u, p.d_err);
+                const int st = j % kStages;
+                const int sbuf = j & 1;
+                wait_or_flag(&kv_full[st], (uint32_t)(j / kStages) & 1u, p.d_err);
+                if (j >= 2) wait_or_flag(&s_free[sbuf], (uint32_t)((j - 2) >> 1) & 1u, p.d_err);
                 tc_fence_after();
                 const uint32_t k_s = sb + kOffKV + st * kStageBytes;
 #pragma unroll
                 for (int kk = 0; kk < 8; ++kk) {
-                    const uint32_t off = (kk >> 2) * kHalfBytes + (kk & 3) * 32;
-                    mma_f16(tS0 + st * 128, smem_desc(q_s + off, 16, 1024), smem_desc(k_s + off, 16, 1024),
-                            idesc_qk, kk > 0);
+                    mma_f16(tS0 + sbuf * kNK, smem_desc(q_s + (kk >> 2) * kQHalf + (kk & 3) * 32, 16, 1024),
+                            smem_desc(k_s + (kk >> 2) * kKVHalf + (kk & 3) * 32, 16, 1024), idesc_qk, kk > 0);
                 }
-                mma_commit(&s_full[st]);
+                mma_commit(&s_full[sbuf]);
                 if (j >= 1) issue_pv(j - 1);
             }
             issue_pv(ntiles - 1);
@@ -286,7 +295,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int c = 0; c < 16; ++c) {
                 const uint4 v = valid ? src[c] : make_uint4(0, 0, 0, 0);
-                const uint32_t dst = sb + kOffQ + (c >> 3) * kHalfBytes + t * 128 + (((c & 7) ^ (t & 7)) << 4);
+                const uint32_t dst = sb + kOffQ + (c >> 3) * kQHalf + t * 128 + (((c & 7) ^ (t & 7)) << 4);
                 asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(dst), "r"(v.x), "r"(v.y), "r"(v.z),
                              "r"(v.w)
                              : "memory");
@@ -303,11 +312,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int st = j & 1;
             wait_or_flag(&s_full[st], (uint32_t)(j >> 1) & 1u, p.d_err);
             tc_fence_after();
-            float s[128];
+            float s[kNK];
 #pragma unroll
-            for (int c = 0; c < 4; ++c) {
+            for (int c = 0; c < kNK / 32; ++c) {
                 float v[32];
-                tmem_ld32(tS0 + st * 128 + lane_off + c * 32, v);
+                tmem_ld32(tS0 + st * kNK + lane_off + c * 32, v);
 #pragma unroll
                 for (int e = 0; e < 32; ++e) s[c * 32 + e] = v[e];
             }
@@ -319,13 +328,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int kb = j * kNK;
             if (kb + kNK - 1 > plim_cta) {
 #pragma unroll
-                for (int c = 0; c < 128; ++c) s[c] = (kb + c <= plim) ? s[c] : -INFINITY;
+                for (int c = 0; c < kNK; ++c) s[c] = (kb + c <= plim) ? s[c] : -INFINITY;
             }
             float mx8[8];
 #pragma unroll
             for (int e = 0; e < 8; ++e) mx8[e] = s[e];
 #pragma unroll
-            for (int c = 8; c < 128; ++c) mx8[c & 7] = fmaxf(mx8[c & 7], s[c]);
+            for (int c = 8; c < kNK; ++c) mx8[c & 7] = fmaxf(mx8[c & 7], s[c]);
             float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
                              fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
             mx *= csc;
@@ -359,9 +368,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             // P row t = 2^(s*scale - max), rounded to the input type, swizzled K-major
             const float neg_m = -m_run;
-            const uint32_t pbase = sb + kOffP + pb * kTileBytes;
+            const uint32_t pbase = sb + kOffP + pb * kPBytes;
 #pragma unroll
-            for (int c = 0; c < 16; ++c) {
+            for (int c = 0; c < kNK / 8; ++c) {
                 float pr[8];
 #pragma unroll
                 for (int e = 0; e < 8; ++e) {
@@ -369,10 +378,24 @@ __global__ void __launch_bounds__(kThreads, 1)
                     l8[e] += pr[e];
                 }
                 const uint4 u = pack8<T>(pr);
-                const uint32_t dst = pbase + (c >> 3) * kHalfBytes + t * 128 + (((c & 7) ^ (t & 7)) << 4);
+                const uint32_t dst = pbase + t * 128 + ((c ^ (t & 7)) << 4);
                 asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(dst), "r"(u.x), "r"(u.y), "r"(u.z),
                              "r"(u.w)
                              : "memory");
+            }
+            if (j == ntiles - 1 && kb + kNK - 1 > kend) {
+                // V rows past the last key any row sees hold whatever the pool
+                // has there (possibly NaN, and 0 * NaN poisons O): zero them
+                const int st_kv = j % kStages;
+                wait_or_flag(&kv_full[st_kv], (uint32_t)(j / kStages) & 1u, p.d_err);
+                const int z0 = kend + 1 - kb;
+                const uint32_t v_s = sb + kOffKV + st_kv * kStageBytes + kKVTile;
+                for (int idx = t; idx < (kNK - z0) * 16; idx += 128) {
+                    const int r = z0 + (idx >> 4), h = (idx >> 3) & 1, c = idx & 7;
+                    asm volatile("st.shared.v4.u32 [%0], {%1,%1,%1,%1};" ::"r"(v_s + h * kKVHalf + r * 128 + c * 16),
+                                 "r"(0u)
+                                 : "memory");
+                }
             }
             asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
             tc_fence_before();

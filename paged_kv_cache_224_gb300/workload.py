@@ -298,13 +298,29 @@ class PrefillCase:
     def kv_bytes(self) -> int:
         return (self.prefix_len + self.chunk_len) * 2 * self.num_kv_heads * self.head_dim * 2
 
-    def materialize(self, device="cpu") -> dict:
+    def materialize(self, device="cpu", pool_fill: Optional[float] = None) -> dict:
+        """Draw the value tensors on ``device`` (seeded) and return them.
+
+        ``pool_fill`` replaces every slot past position P+C-1 (unowned blocks
+        and the tail of the last block) with this constant -- NaN garbage.
+        """
         g = torch.Generator(device=device)
         g.manual_seed(self.seed)
         dt = TORCH_DTYPES[self.dtype]
         shape = (self.num_blocks, self.num_kv_heads, self.block_size, self.head_dim)
         kc = torch.randn(shape, generator=g, device=device, dtype=dt)
         vc = torch.randn(shape, generator=g, device=device, dtype=dt)
+        if pool_fill is not None:
+            bs, end = self.block_size, self.prefix_len + self.chunk_len
+            owned = torch.zeros(self.num_blocks, dtype=torch.bool)
+            owned[torch.as_tensor(self.block_table, dtype=torch.long)] = True
+            unowned = (~owned).nonzero().flatten().to(device)
+            kc[unowned] = pool_fill
+            vc[unowned] = pool_fill
+            if end % bs:
+                blk = int(self.block_table[end // bs])
+                kc[blk, :, end % bs:, :] = pool_fill
+                vc[blk, :, end % bs:, :] = pool_fill
         C = self.chunk_len
         q = torch.randn((C, self.num_heads, self.head_dim), generator=g, device=device, dtype=dt)
         nk = torch.randn((C, self.num_kv_heads, self.head_dim), generator=g, device=device, dtype=dt)

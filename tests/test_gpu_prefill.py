@@ -112,3 +112,18 @@ def test_chunkwise_cache_writes_are_bit_identical_to_one_write():
                                 slots[a:b].contiguous())
     torch.cuda.synchronize()
     assert torch.equal(kc1, kc2) and torch.equal(vc1, vc2)
+
+
+@pytest.mark.parametrize("P,C,G,bs", [(37, 20, 4, 16), (500, 45, 8, 32), (0, 5, 1, 16)])
+def test_prefill_ignores_nan_garbage_past_the_chunk(P, C, G, bs):
+    # every slot past position P+C-1 holds NaN: only keys 0..P+i may reach row i
+    case = wl.make_prefill_case(f"pfnan{P}_{C}", P, C, 2 * G, 2, 128, bs, "bf16", seed=900 + P + C)
+    t = case.materialize(DEV, pool_fill=float("nan"))
+    kc, vc = wl.bits(t["k_cache"]), wl.bits(t["v_cache"])
+    assert oracle.reshape_and_cache(wl.bits(t["new_key"]), wl.bits(t["new_value"]), kc, vc,
+                                    case.slot_mapping, bs) == 0
+    ref = oracle.prefill_chunk(wl.bits(t["query"]), kc, vc, case.block_table, P, case.scale, "bf16",
+                               num_threads=8)
+    out = run_prefill(case, t)
+    assert torch.isfinite(out.float()).all()
+    check_attention(to_f64(out), ref, "bf16", case.name)
