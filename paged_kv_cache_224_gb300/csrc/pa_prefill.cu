@@ -16,8 +16,8 @@
 //   warps 2-5 softmax: each thread owns one query row = one TMEM lane; reads
 //             its S row, applies the causal mask, updates the running max
 //             (rescaling O in TMEM only when the max grows by more than 2^8),
-//             writes P (rounded to the input type) into one of two shared
-//             buffers for the PV MMA, and finally normalises O and stores the
+//             writes P (rounded to the input type) into one of two TMEM
+//             buffers, the A operand of the PV MMA, and finally normalises O and stores the
 //             row.  With two P buffers the softmax of tile j overlaps PV of
 //             tile j-1; it waits for that PV only when O must be rescaled.
 //             On the last tile it zeroes the V rows past the CTA's last key,
@@ -41,16 +41,15 @@ constexpr int kQHalf = kM * 128;               // one 64-dim half of Q: 128 rows
 constexpr int kKVHalf = kNK * 128;             // one 64-dim half of a K or V tile
 constexpr int kKVTile = 2 * kKVHalf;           // 16 KB
 constexpr int kStageBytes = 2 * kKVTile;       // K tile + V tile
-constexpr int kPBytes = kM * kNK * 2;          // P: 128 rows x 64 keys = one 128-byte-wide half
 constexpr int kOffQ = 0;
 constexpr int kOffKV = kOffQ + 2 * kQHalf;                 // 32 KB
-constexpr int kOffP = kOffKV + kStages * kStageBytes;      // 160 KB, two P buffers
-constexpr int kOffBar = kOffP + 2 * kPBytes;               // 192 KB
+constexpr int kOffBar = kOffKV + kStages * kStageBytes;    // 160 KB
 constexpr int kSmemUsed = kOffBar + 256;
 constexpr int kSmemAlloc = kSmemUsed + 1024;               // room to align the base to 1 KB
 constexpr int kThreads = 192;
-constexpr uint32_t kTmemCols = 256;                        // S0, S1 (64 columns each), O (128)
-static_assert(kNK * 2 == 128, "P rows are one 128-byte swizzle row");
+// TMEM columns: S0, S1 (64 fp32 each), P0, P1 (64 keys as 32 packed pairs each), O (128 fp32)
+constexpr uint32_t kColS = 0, kColP = 128, kColO = 256;
+constexpr uint32_t kTmemCols = 512;
 
 // ---- tcgen05 / TMA wrappers (inline PTX) ---------------------------------
 
@@ -84,6 +83,16 @@ __device__ __forceinline__ void mma_f16(uint32_t tmem_d, uint64_t adesc, uint64_
         : "memory");
 }
 
+// Same, with A read from tensor memory (row i in lane i, K pairs packed per column).
+__device__ __forceinline__ void mma_f16_ts(uint32_t tmem_d, uint32_t tmem_a, uint64_t bdesc, uint32_t idesc,
+                                           bool accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(tmem_d),
+        "r"(tmem_a), "l"(bdesc), "r"(idesc), "r"((uint32_t)accumulate)
+        : "memory");
+}
+
 __device__ __forceinline__ void mma_commit(uint64_t *bar) {
     asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
                      smem_addr(bar))
@@ -103,6 +112,17 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
         : "r"(taddr));
 #pragma unroll
     for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+__device__ __forceinline__ void tmem_st32u(uint32_t taddr, const uint32_t (&r)[32]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+        "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
+        "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]),
+        "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]), "r"(r[16]),
+        "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]), "r"(r[24]),
+        "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
+        : "memory");
 }
 
 __device__ __forceinline__ void tmem_st32(uint32_t taddr, const float (&v)[32]) {
@@ -200,7 +220,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_holder;
-    const uint32_t tS0 = tmem, tO = tmem + 2 * kNK;
+    const uint32_t tS0 = tmem + kColS, tP0 = tmem + kColP, tO = tmem + kColO;
 
     if (warp == 0) {
         // ============================================================ producer
@@ -246,13 +266,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int stage = jj % kStages;
                 wait_or_flag(&p_full[pb], (uint32_t)(jj >> 1) & 1u, p.d_err);
                 tc_fence_after();
-                const uint32_t p_s = sb + kOffP + pb * kPBytes;
                 const uint32_t v_s = sb + kOffKV + stage * kStageBytes + kKVTile;
 #pragma unroll
                 for (int kk = 0; kk < kNK / 16; ++kk) {
-                    const uint64_t a = smem_desc(p_s + kk * 32, 16, 1024);
                     const uint64_t b = smem_desc(v_s + kk * 2048, kKVHalf, 1024);
-                    mma_f16(tO, a, b, idesc_pv, jj > 0 || kk > 0);
+                    mma_f16_ts(tO, tP0 + pb * (kNK / 2) + kk * 8, b, idesc_pv, jj > 0 || kk > 0);
                 }
                 mma_commit(&pv_done[pb]);
                 mma_commit(&kv_empty[stage]);
@@ -366,9 +384,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 m_run = mx;
             }
-            // P row t = 2^(s*scale - max), rounded to the input type, swizzled K-major
+            // P row t = 2^(s*scale - max), rounded to the input type, into TMEM lane t
             const float neg_m = -m_run;
-            const uint32_t pbase = sb + kOffP + pb * kPBytes;
+            uint32_t pk[kNK / 2];
 #pragma unroll
             for (int c = 0; c < kNK / 8; ++c) {
                 float pr[8];
@@ -378,11 +396,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                     l8[e] += pr[e];
                 }
                 const uint4 u = pack8<T>(pr);
-                const uint32_t dst = pbase + t * 128 + ((c ^ (t & 7)) << 4);
-                asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(dst), "r"(u.x), "r"(u.y), "r"(u.z),
-                             "r"(u.w)
-                             : "memory");
+                pk[c * 4 + 0] = u.x;
+                pk[c * 4 + 1] = u.y;
+                pk[c * 4 + 2] = u.z;
+                pk[c * 4 + 3] = u.w;
             }
+            tmem_st32u(tP0 + pb * (kNK / 2) + lane_off, pk);
             if (j == ntiles - 1 && kb + kNK - 1 > kend) {
                 // V rows past the last key any row sees hold whatever the pool
                 // has there (possibly NaN, and 0 * NaN poisons O): zero them
@@ -396,8 +415,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                                  "r"(0u)
                                  : "memory");
                 }
+                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
             }
-            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            tmem_wait_st();
             tc_fence_before();
             mbar_arrive1(&p_full[pb]);
         }
