@@ -6,22 +6,29 @@
 // prefix_len + i and sees keys 0 .. prefix_len + i, gathered through the
 // block table.
 //
-// One CTA computes 128 query rows -- 128/G chunk positions times the G query
-// heads of one kv head -- against 64-key tiles:
+// One CTA computes two tiles of 128 query rows -- 256/G chunk positions times
+// the G query heads of one kv head -- against 128-key tiles that both Q tiles
+// share (each K/V byte brought into shared memory serves 256 rows):
 //   warp 0    TMA producer: for each key tile, one 2-D tensor copy per
 //             (block, 64-dim half) of K and of V, straight from the paged pool
-//             into a 128-byte-swizzled shared layout (four stages in flight);
-//   warp 1    MMA issuer (one thread): S = Q K^T into TMEM (two buffers), then
-//             O += P V into TMEM, tcgen05.mma kind::f16, fp32 accumulation;
-//   warps 2-5 softmax: each thread owns one query row = one TMEM lane; reads
-//             its S row, applies the causal mask, updates the running max
-//             (rescaling O in TMEM only when the max grows by more than 2^8),
-//             writes P (rounded to the input type) into one of two TMEM
-//             buffers, the A operand of the PV MMA, and finally normalises O and stores the
-//             row.  With two P buffers the softmax of tile j overlaps PV of
-//             tile j-1; it waits for that PV only when O must be rescaled.
-//             On the last tile it zeroes the V rows past the CTA's last key,
-//             so garbage (even NaN) in unused slots never reaches O.
+//             into a 128-byte-swizzled shared layout (two stages);
+//             block-table entries are read 32 at a time, a chunk ahead;
+//   warp 1    MMA issuer (one thread): per key tile j and Q tile g, first
+//             O_g += P_g(j-1) V(j-1), then S_g = Q_g K(j)^T, tcgen05.mma
+//             kind::f16 with fp32 accumulation in TMEM.  P_g is written over
+//             the first half of S_g's TMEM columns and read from there as the
+//             A operand; the tensor pipe runs one thread's MMAs in order, so
+//             the PV of tile j-1 has read P before the QK of tile j writes S,
+//             and S_g(j) being complete means O_g holds every PV up to j-1;
+//   warps 2-5 softmax of Q tile 0, warps 6-9 of Q tile 1: each thread owns one
+//             query row = one TMEM lane; it reads its S row, applies the causal
+//             mask, updates the running max (rescaling O in TMEM only when the
+//             max grows by more than 2^8), writes P (rounded to the input
+//             type) into TMEM, and finally normalises O and stores the row.
+//             The two groups interleave, so the tensor pipe works on one Q
+//             tile's MMAs while the other's softmax runs.  On the last key tile
+//             each group zeroes the V rows past the CTA's last key, so garbage
+//             (even NaN) in unused slots never reaches O.
 // All waits are bounded; a wait that gives up flags PA_DEVERR_TIMEOUT.
 #include <cuda.h>
 
@@ -34,21 +41,24 @@ namespace pa {
 namespace {
 
 constexpr int kD = 128;                        // head_dim
-constexpr int kM = 128;                        // query rows per CTA
-constexpr int kNK = 64;                        // keys per tile
-constexpr int kStages = 4;                     // K/V tiles in flight
-constexpr int kQHalf = kM * 128;               // one 64-dim half of Q: 128 rows x 128 bytes
+constexpr int kM = 128;                        // query rows per Q tile (one per TMEM lane)
+constexpr int kQT = 2;                         // Q tiles per CTA
+constexpr int kNK = 128;                       // keys per tile
+constexpr int kStages = 2;                     // K/V tiles in flight
+constexpr int kQHalf = kM * 128;               // one 64-dim half of a Q tile: 128 rows x 128 bytes
+constexpr int kQTile = 2 * kQHalf;             // 32 KB
 constexpr int kKVHalf = kNK * 128;             // one 64-dim half of a K or V tile
-constexpr int kKVTile = 2 * kKVHalf;           // 16 KB
+constexpr int kKVTile = 2 * kKVHalf;           // 32 KB
 constexpr int kStageBytes = 2 * kKVTile;       // K tile + V tile
 constexpr int kOffQ = 0;
-constexpr int kOffKV = kOffQ + 2 * kQHalf;                 // 32 KB
-constexpr int kOffBar = kOffKV + kStages * kStageBytes;    // 160 KB
+constexpr int kOffKV = kOffQ + kQT * kQTile;               // 64 KB
+constexpr int kOffBar = kOffKV + kStages * kStageBytes;    // 192 KB
 constexpr int kSmemUsed = kOffBar + 256;
 constexpr int kSmemAlloc = kSmemUsed + 1024;               // room to align the base to 1 KB
-constexpr int kThreads = 192;
-// TMEM columns: S0, S1 (64 fp32 each), P0, P1 (64 keys as 32 packed pairs each), O (128 fp32)
-constexpr uint32_t kColS = 0, kColP = 128, kColO = 256;
+constexpr int kThreads = 64 + kQT * 128;
+// TMEM columns: S of each Q tile (128 fp32; P overwrites its first 64 columns
+// as 128 packed pairs), O of each Q tile (128 fp32)
+constexpr uint32_t kColS = 0, kColO = 256;
 constexpr uint32_t kTmemCols = 512;
 
 // ---- tcgen05 / TMA wrappers (inline PTX) ---------------------------------
@@ -56,16 +66,17 @@ constexpr uint32_t kTmemCols = 512;
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
 
-// Shared-memory matrix descriptor: start, leading / stride byte offsets,
-// descriptor version 1, 128-byte swizzle.
-__device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
-    uint64_t d = (uint64_t)((saddr >> 4) & 0x3FFF);
-    d |= (uint64_t)((lbo >> 4) & 0x3FFF) << 16;
-    d |= (uint64_t)((sbo >> 4) & 0x3FFF) << 32;
-    d |= (uint64_t)1 << 46;
-    d |= (uint64_t)2 << 61;
-    return d;
+// Shared-memory matrix descriptor, split in 32-bit halves so that the issuing
+// thread only adds an offset per MMA.  Low word: start address >> 4 (bits
+// 0-13) and leading byte offset >> 4 (bits 16-29); high word: stride byte
+// offset >> 4 (bits 32-45), descriptor version 1 (bit 46), 128-byte swizzle
+// (value 2 at bit 61).  Shared addresses stay below 2^18, so adding
+// (offset >> 4) to the low word never carries out of the start field.
+__device__ __forceinline__ uint32_t desc_lo(uint32_t saddr, uint32_t lbo) {
+    return ((saddr >> 4) & 0x3FFFu) | (((lbo >> 4) & 0x3FFFu) << 16);
 }
+__host__ __device__ constexpr uint32_t desc_hi(uint32_t sbo) { return ((sbo >> 4) & 0x3FFFu) | (1u << 14) | (2u << 29); }
+__device__ __forceinline__ uint64_t desc_of(uint32_t lo, uint32_t hi) { return ((uint64_t)hi << 32) | lo; }
 
 // Instruction descriptor, kind::f16: fp32 accumulator, A and B both fp16 or
 // both bf16, A K-major, B K-major or MN-major, M = 128, N given.
@@ -170,7 +181,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                       const __grid_constant__ CUtensorMap tmv) {
     constexpr bool kBf16 = std::is_same<T, __nv_bfloat16>::value;
     constexpr int kBlocksPerTile = kNK / BS;
-    static_assert(kNK % BS == 0 && kBlocksPerTile <= 32, "block_size");
+    static_assert(kNK % BS == 0 && kBlocksPerTile <= 32 && 32 % kBlocksPerTile == 0, "block_size");
     static_assert(kM % G == 0, "group");
 
     extern __shared__ unsigned char smem_raw[];
@@ -178,20 +189,20 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t sb = (raw + 1023u) & ~1023u;  // 1 KB aligned: swizzle atoms start on 1 KB
     unsigned char *gb = smem_raw + (sb - raw);
     uint64_t *bars = reinterpret_cast<uint64_t *>(gb + kOffBar);
-    uint64_t *kv_full = bars + 0;   // [kStages] TMA -> MMA
-    uint64_t *kv_empty = bars + 4;  // [kStages] MMA -> TMA
-    uint64_t *q_full = bars + 8;    // softmax threads -> MMA (Q tile written)
-    uint64_t *s_full = bars + 9;    // [2] MMA -> softmax (S ready)
-    uint64_t *s_free = bars + 11;   // [2] softmax -> MMA (S read)
-    uint64_t *p_full = bars + 13;   // [2] softmax -> MMA (P buffer written, O rescaled)
-    uint64_t *pv_done = bars + 15;  // [2] MMA -> softmax (PV of that P buffer finished)
-    volatile uint32_t *tmem_holder = reinterpret_cast<volatile uint32_t *>(bars + 17);
+    uint64_t *kv_full = bars + 0;               // [kStages] TMA -> MMA
+    uint64_t *kv_empty = bars + kStages;        // [kStages] MMA -> TMA
+    uint64_t *q_full = bars + 2 * kStages;      // softmax threads -> MMA (both Q tiles written)
+    uint64_t *s_full = q_full + 1;              // [kQT] MMA -> softmax (S ready, O holds all PVs before it)
+    uint64_t *p_full = s_full + kQT;            // [kQT] softmax -> MMA (S read, P written, O rescaled)
+    uint64_t *o_done = p_full + kQT;            // [kQT] MMA -> softmax (last PV finished)
+    volatile uint32_t *tmem_holder = reinterpret_cast<volatile uint32_t *>(o_done + kQT);
+    static_assert((2 * kStages + 1 + 3 * kQT + 1) * 8 <= kSmemUsed - kOffBar, "barrier area");
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int kvh = blockIdx.y;
-    const int row0 = blockIdx.x * kM;
+    const int row0 = blockIdx.x * (kQT * kM);
     const int nrows = p.chunk_len * G;
-    const int i_last = min(p.chunk_len - 1, (row0 + kM - 1) / G);
+    const int i_last = min(p.chunk_len - 1, (row0 + kQT * kM - 1) / G);
     const int kend = p.prefix_len + i_last;  // last key any row of this CTA sees
     const int ntiles = kend / kNK + 1;
 
@@ -200,13 +211,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(&kv_full[i], 1);
             mbar_init(&kv_empty[i], 1);
         }
-        for (int i = 0; i < 2; ++i) {
-            mbar_init(&s_full[i], 1);
-            mbar_init(&s_free[i], 128);
-            mbar_init(&p_full[i], 128);
-            mbar_init(&pv_done[i], 1);
+        mbar_init(q_full, kQT * 128);
+        for (int g = 0; g < kQT; ++g) {
+            mbar_init(&s_full[g], 1);
+            mbar_init(&p_full[g], 128);
+            mbar_init(&o_done[g], 1);
         }
-        mbar_init(q_full, 128);
         fence_barrier_init();
     }
     if (warp == 1) {
@@ -220,22 +230,25 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_holder;
-    const uint32_t tS0 = tmem + kColS, tP0 = tmem + kColP, tO = tmem + kColO;
 
     if (warp == 0) {
         // ============================================================ producer
         const int32_t *table = p.block_table;
         const int oob_row = p.num_blocks * p.num_kv_heads * BS;  // first row past the pool: zero fill
-        // lane b < kBlocksPerTile handles block b of each tile; entries load one tile ahead
-        auto entry = [&](int jt) {
-            const int key0 = jt * kNK + lane * BS;
-            return (lane < kBlocksPerTile && key0 <= kend) ? table[key0 / BS] : -1;
-        };
-        int blk_next = entry(0);
+        // Table entries come 32 at a time, one per lane, a whole chunk ahead of
+        // use (a chunk covers 32 / kBlocksPerTile tiles), so the producer never
+        // waits on a table load; lane b < kBlocksPerTile handles block b of a tile.
+        const int nent = kend / BS + 1;
+        auto chunk = [&](int c) { return c * 32 + lane < nent ? table[c * 32 + lane] : -1; };
+        int ent_cur = chunk(0), ent_nxt = chunk(1);
+        constexpr int kTilesPerChunk = 32 / kBlocksPerTile;
         for (int j = 0; j < ntiles; ++j) {
             const int st = j % kStages;
-            const int blk = blk_next;
-            if (j + 1 < ntiles) blk_next = entry(j + 1);
+            if (j > 0 && j % kTilesPerChunk == 0) {
+                ent_cur = ent_nxt;
+                ent_nxt = chunk(j / kTilesPerChunk + 1);
+            }
+            const int blk = __shfl_sync(0xffffffffu, ent_cur, (j % kTilesPerChunk) * kBlocksPerTile + (lane % kBlocksPerTile));
             int y = oob_row;
             if (lane < kBlocksPerTile && j * kNK + lane * BS <= kend) {
                 if (blk >= 0 && blk < p.num_blocks) y = (blk * p.num_kv_heads + kvh) * BS;
@@ -260,60 +273,74 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) {
             constexpr uint32_t idesc_qk = instr_desc(kBf16, false, kNK);
             constexpr uint32_t idesc_pv = instr_desc(kBf16, true, kD);
-            const uint32_t q_s = sb + kOffQ;
-            auto issue_pv = [&](int jj) {
-                const int pb = jj & 1;
-                const int stage = jj % kStages;
-                wait_or_flag(&p_full[pb], (uint32_t)(jj >> 1) & 1u, p.d_err);
-                tc_fence_after();
-                const uint32_t v_s = sb + kOffKV + stage * kStageBytes + kKVTile;
-#pragma unroll
-                for (int kk = 0; kk < kNK / 16; ++kk) {
-                    const uint64_t b = smem_desc(v_s + kk * 2048, kKVHalf, 1024);
-                    mma_f16_ts(tO, tP0 + pb * (kNK / 2) + kk * 8, b, idesc_pv, jj > 0 || kk > 0);
-                }
-                mma_commit(&pv_done[pb]);
-                mma_commit(&kv_empty[stage]);
-            };
+            constexpr uint32_t hi = desc_hi(1024);
+            // descriptor low words of Q tile 0 and of stage 0's K and V; the
+            // rest are fixed offsets from these
+            const uint32_t q_lo0 = desc_lo(sb + kOffQ, 16);
+            const uint32_t k_lo0 = desc_lo(sb + kOffKV, 16);
+            const uint32_t v_lo0 = desc_lo(sb + kOffKV + kKVTile, kKVHalf);
             wait_or_flag(q_full, 0, p.d_err);
             tc_fence_after();
-            for (int j = 0; j < ntiles; ++j) {
-                const int st = j % kStages;
-                const int sbuf = j & 1;
-                wait_or_flag(&kv_full[st], (uint32_t)(j / kStages) & 1u, p.d_err);
-                if (j >= 2) wait_or_flag(&s_free[sbuf], (uint32_t)((j - 2) >> 1) & 1u, p.d_err);
-                tc_fence_after();
-                const uint32_t k_s = sb + kOffKV + st * kStageBytes;
-#pragma unroll
-                for (int kk = 0; kk < 8; ++kk) {
-                    mma_f16(tS0 + sbuf * kNK, smem_desc(q_s + (kk >> 2) * kQHalf + (kk & 3) * 32, 16, 1024),
-                            smem_desc(k_s + (kk >> 2) * kKVHalf + (kk & 3) * 32, 16, 1024), idesc_qk, kk > 0);
+            for (int j = 0; j <= ntiles; ++j) {
+                const int st = j % kStages, stp = (j + kStages - 1) % kStages;
+                if (j < ntiles) {
+                    wait_or_flag(&kv_full[st], (uint32_t)(j / kStages) & 1u, p.d_err);
+                    tc_fence_after();
                 }
-                mma_commit(&s_full[sbuf]);
-                if (j >= 1) issue_pv(j - 1);
+#pragma unroll
+                for (int g = 0; g < kQT; ++g) {
+                    const uint32_t tS = tmem + kColS + g * kNK;
+                    if (j >= 1) {
+                        // O_g += P_g(j-1) V(j-1); P sits in S_g's first 64 columns
+                        wait_or_flag(&p_full[g], (uint32_t)(j - 1) & 1u, p.d_err);
+                        tc_fence_after();
+                        const uint32_t v_lo = v_lo0 + stp * (kStageBytes >> 4);
+#pragma unroll
+                        for (int kk = 0; kk < kNK / 16; ++kk)
+                            mma_f16_ts(tmem + kColO + g * kD, tS + kk * 8, desc_of(v_lo + kk * (2048 >> 4), hi),
+                                       idesc_pv, j > 1 || kk > 0);
+                        if (j == ntiles) mma_commit(&o_done[g]);
+                        if (g == kQT - 1) mma_commit(&kv_empty[stp]);
+                    }
+                    if (j < ntiles) {
+                        // S_g = Q_g K(j)^T
+                        const uint32_t q_lo = q_lo0 + g * (kQTile >> 4);
+                        const uint32_t k_lo = k_lo0 + st * (kStageBytes >> 4);
+#pragma unroll
+                        for (int kk = 0; kk < 8; ++kk) {
+                            const uint32_t qo = ((kk >> 2) * kQHalf + (kk & 3) * 32) >> 4;
+                            const uint32_t ko = ((kk >> 2) * kKVHalf + (kk & 3) * 32) >> 4;
+                            mma_f16(tS, desc_of(q_lo + qo, hi), desc_of(k_lo + ko, hi), idesc_qk, kk > 0);
+                        }
+                        mma_commit(&s_full[g]);
+                    }
+                }
             }
-            issue_pv(ntiles - 1);
         }
     } else {
         // ============================================================ softmax
-        const int quarter = warp & 3;
-        const int t = quarter * 32 + lane;  // query row of this thread = TMEM lane
+        const int g = (warp - 2) >> 2;         // Q tile of this warp group
+        const int quarter = warp & 3;          // TMEM lanes 32*quarter .. +31 (fixed by the warp id)
+        const int t = quarter * 32 + lane;     // query row of this thread within its Q tile = TMEM lane
         const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
-        const int gr = row0 + t;
+        const int gr = row0 + g * kM + t;
         const bool valid = gr < nrows;
         const int ipos = valid ? gr / G : 0, head = valid ? gr % G : 0;
         const int plim = p.prefix_len + min(gr / G, p.chunk_len - 1);
-        const int plim_cta = p.prefix_len + row0 / G;  // smallest limit of any row in the CTA
-        const float csc = p.scale_log2;                 // > 0 (checked on the host)
+        const int plim_min = p.prefix_len + min((row0 + g * kM) / G, p.chunk_len - 1);  // smallest limit in the tile
+        const float csc = p.scale_log2;                   // > 0 (checked on the host)
+        const uint32_t tS = tmem + kColS + g * kNK + lane_off;
+        const uint32_t tO = tmem + kColO + g * kD + lane_off;
 
-        // Q row t into the swizzled K-major tile
+        // Q row t into the swizzled K-major tile of this group
         {
             const uint4 *src = reinterpret_cast<const uint4 *>(static_cast<const T *>(p.query) +
                                                                ((size_t)ipos * p.num_heads + kvh * G + head) * kD);
 #pragma unroll
             for (int c = 0; c < 16; ++c) {
                 const uint4 v = valid ? src[c] : make_uint4(0, 0, 0, 0);
-                const uint32_t dst = sb + kOffQ + (c >> 3) * kQHalf + t * 128 + (((c & 7) ^ (t & 7)) << 4);
+                const uint32_t dst =
+                    sb + kOffQ + g * kQTile + (c >> 3) * kQHalf + t * 128 + (((c & 7) ^ (t & 7)) << 4);
                 asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(dst), "r"(v.x), "r"(v.y), "r"(v.z),
                              "r"(v.w)
                              : "memory");
@@ -327,81 +354,93 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int e = 0; e < 8; ++e) l8[e] = 0.f;
         for (int j = 0; j < ntiles; ++j) {
-            const int st = j & 1;
-            wait_or_flag(&s_full[st], (uint32_t)(j >> 1) & 1u, p.d_err);
+            wait_or_flag(&s_full[g], (uint32_t)j & 1u, p.d_err);
             tc_fence_after();
-            float s[kNK];
-#pragma unroll
-            for (int c = 0; c < kNK / 32; ++c) {
-                float v[32];
-                tmem_ld32(tS0 + st * kNK + lane_off + c * 32, v);
-#pragma unroll
-                for (int e = 0; e < 32; ++e) s[c * 32 + e] = v[e];
-            }
-            tmem_wait_ld();
-            tc_fence_before();
-            mbar_arrive1(&s_free[st]);
-
             // causal mask only on tiles that reach past some row's limit
             const int kb = j * kNK;
-            if (kb + kNK - 1 > plim_cta) {
-#pragma unroll
-                for (int c = 0; c < kNK; ++c) s[c] = (kb + c <= plim) ? s[c] : -INFINITY;
-            }
+            const bool need_mask = kb + kNK - 1 > plim_min;
+            // pass 1: row max, 64 columns at a time (128 live values would spill)
             float mx8[8];
 #pragma unroll
-            for (int e = 0; e < 8; ++e) mx8[e] = s[e];
+            for (int e = 0; e < 8; ++e) mx8[e] = -INFINITY;
+#pragma unroll 1
+            for (int h = 0; h < 2; ++h) {
+                float s0[32], s1[32];
+                tmem_ld32(tS + h * 64, s0);
+                tmem_ld32(tS + h * 64 + 32, s1);
+                tmem_wait_ld();
+                float s[64];
 #pragma unroll
-            for (int c = 8; c < kNK; ++c) mx8[c & 7] = fmaxf(mx8[c & 7], s[c]);
+                for (int e = 0; e < 32; ++e) {
+                    s[e] = s0[e];
+                    s[32 + e] = s1[e];
+                }
+                if (need_mask) {
+#pragma unroll
+                    for (int c = 0; c < 64; ++c) s[c] = (kb + h * 64 + c <= plim) ? s[c] : -INFINITY;
+                }
+#pragma unroll
+                for (int c = 0; c < 64; ++c) mx8[c & 7] = fmaxf(mx8[c & 7], s[c]);
+            }
             float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
                              fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
             mx *= csc;
 
-            // the P buffer of this tile was last read by PV of tile j-2
-            const int pb = j & 1;
-            if (j >= 2) {
-                wait_or_flag(&pv_done[pb], (uint32_t)((j - 2) >> 1) & 1u, p.d_err);
-                tc_fence_after();
-            }
             if (mx > m_run + 8.0f) {
                 if (j >= 1 && m_run != -INFINITY) {
-                    // O must hold every PV so far before it is rescaled
-                    wait_or_flag(&pv_done[(j - 1) & 1], (uint32_t)((j - 1) >> 1) & 1u, p.d_err);
-                    tc_fence_after();
+                    // S(j) complete means O holds every PV before it: rescale in place
                     const float alpha = fast_exp2(m_run - mx);
 #pragma unroll
                     for (int c = 0; c < 4; ++c) {
                         float v[32];
-                        tmem_ld32(tO + lane_off + c * 32, v);
+                        tmem_ld32(tO + c * 32, v);
                         tmem_wait_ld();
 #pragma unroll
                         for (int e = 0; e < 32; ++e) v[e] *= alpha;
-                        tmem_st32(tO + lane_off + c * 32, v);
+                        tmem_st32(tO + c * 32, v);
                     }
-                    tmem_wait_st();
 #pragma unroll
                     for (int e = 0; e < 8; ++e) l8[e] *= alpha;
                 }
                 m_run = mx;
             }
-            // P row t = 2^(s*scale - max), rounded to the input type, into TMEM lane t
+            // pass 2: P row t = 2^(s*scale - max), rounded to the input type,
+            // packed over S's first 64 columns (half h goes to columns 32h..32h+31,
+            // which pass 2 of half h-1 has already read)
             const float neg_m = -m_run;
-            uint32_t pk[kNK / 2];
+#pragma unroll 1
+            for (int h = 0; h < 2; ++h) {
+                float s0[32], s1[32];
+                tmem_ld32(tS + h * 64, s0);
+                tmem_ld32(tS + h * 64 + 32, s1);
+                tmem_wait_ld();
+                float s[64];
 #pragma unroll
-            for (int c = 0; c < kNK / 8; ++c) {
-                float pr[8];
-#pragma unroll
-                for (int e = 0; e < 8; ++e) {
-                    pr[e] = fast_exp2(fmaf(s[c * 8 + e], csc, neg_m));
-                    l8[e] += pr[e];
+                for (int e = 0; e < 32; ++e) {
+                    s[e] = s0[e];
+                    s[32 + e] = s1[e];
                 }
-                const uint4 u = pack8<T>(pr);
-                pk[c * 4 + 0] = u.x;
-                pk[c * 4 + 1] = u.y;
-                pk[c * 4 + 2] = u.z;
-                pk[c * 4 + 3] = u.w;
+                if (need_mask) {
+#pragma unroll
+                    for (int c = 0; c < 64; ++c) s[c] = (kb + h * 64 + c <= plim) ? s[c] : -INFINITY;
+                }
+                uint32_t pk[32];
+#pragma unroll
+                for (int c = 0; c < 8; ++c) {
+                    float pr[8];
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) {
+                        pr[e] = fast_exp2(fmaf(s[c * 8 + e], csc, neg_m));
+                        l8[e] += pr[e];
+                    }
+                    const uint4 u = pack8<T>(pr);
+                    pk[c * 4 + 0] = u.x;
+                    pk[c * 4 + 1] = u.y;
+                    pk[c * 4 + 2] = u.z;
+                    pk[c * 4 + 3] = u.w;
+                }
+                tmem_st32u(tS + h * 32, pk);
             }
-            tmem_st32u(tP0 + pb * (kNK / 2) + lane_off, pk);
             if (j == ntiles - 1 && kb + kNK - 1 > kend) {
                 // V rows past the last key any row sees hold whatever the pool
                 // has there (possibly NaN, and 0 * NaN poisons O): zero them
@@ -419,11 +458,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             tmem_wait_st();
             tc_fence_before();
-            mbar_arrive1(&p_full[pb]);
+            mbar_arrive1(&p_full[g]);
         }
 
         // epilogue: O row / l, rounded once, stored
-        wait_or_flag(&pv_done[(ntiles - 1) & 1], (uint32_t)((ntiles - 1) >> 1) & 1u, p.d_err);
+        wait_or_flag(&o_done[g], 0, p.d_err);
         tc_fence_after();
         const float l_run = ((l8[0] + l8[1]) + (l8[2] + l8[3])) + ((l8[4] + l8[5]) + (l8[6] + l8[7]));
         const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
@@ -431,7 +470,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
             float v[32];
-            tmem_ld32(tO + lane_off + c * 32, v);
+            tmem_ld32(tO + c * 32, v);
             tmem_wait_ld();
             if (valid) {
 #pragma unroll
@@ -503,7 +542,7 @@ int launch_tc_t(const PrefillParams &p, cudaStream_t stream) {
     CUtensorMap tmk, tmv;
     if (!make_pool_map(&tmk, p.k_cache, p, BS, bf16) || !make_pool_map(&tmv, p.v_cache, p, BS, bf16))
         return PA_ERR_CUDA;
-    dim3 grid((p.chunk_len * G + kM - 1) / kM, p.num_kv_heads);
+    dim3 grid((p.chunk_len * G + kQT * kM - 1) / (kQT * kM), p.num_kv_heads);
     kern<<<grid, kThreads, kSmemAlloc, stream>>>(p, tmk, tmv);
     return cudaPeekAtLastError() == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }
