@@ -11,8 +11,11 @@
 // share (each K/V byte brought into shared memory serves 256 rows):
 //   warp 0    TMA producer: for each key tile, one 2-D tensor copy per
 //             (block, 64-dim half) of K and of V, straight from the paged pool
-//             into a 128-byte-swizzled shared layout (two stages);
-//             block-table entries are read 32 at a time, a chunk ahead;
+//             into a 128-byte-swizzled shared layout.  K and V have rings of
+//             their own (two stages each): K(j) is free once the QKs of tile
+//             j ran, a whole MMA round before V(j), so K(j+2) streams in while
+//             V(j) is still in use.  Block-table entries are read 32 at a
+//             time, a chunk ahead;
 //   warp 1    MMA issuer (one thread): per key tile j and Q tile g, first
 //             O_g += P_g(j-1) V(j-1), then S_g = Q_g K(j)^T, tcgen05.mma
 //             kind::f16 with fp32 accumulation in TMEM.  P_g is written over
@@ -49,10 +52,10 @@ constexpr int kQHalf = kM * 128;               // one 64-dim half of a Q tile: 1
 constexpr int kQTile = 2 * kQHalf;             // 32 KB
 constexpr int kKVHalf = kNK * 128;             // one 64-dim half of a K or V tile
 constexpr int kKVTile = 2 * kKVHalf;           // 32 KB
-constexpr int kStageBytes = 2 * kKVTile;       // K tile + V tile
 constexpr int kOffQ = 0;
-constexpr int kOffKV = kOffQ + kQT * kQTile;               // 64 KB
-constexpr int kOffBar = kOffKV + kStages * kStageBytes;    // 192 KB
+constexpr int kOffK = kOffQ + kQT * kQTile;                // 64 KB: K ring
+constexpr int kOffV = kOffK + kStages * kKVTile;           // 128 KB: V ring
+constexpr int kOffBar = kOffV + kStages * kKVTile;         // 192 KB
 constexpr int kSmemUsed = kOffBar + 256;
 constexpr int kSmemAlloc = kSmemUsed + 1024;               // room to align the base to 1 KB
 constexpr int kThreads = 64 + kQT * 128;
@@ -189,14 +192,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t sb = (raw + 1023u) & ~1023u;  // 1 KB aligned: swizzle atoms start on 1 KB
     unsigned char *gb = smem_raw + (sb - raw);
     uint64_t *bars = reinterpret_cast<uint64_t *>(gb + kOffBar);
-    uint64_t *kv_full = bars + 0;               // [kStages] TMA -> MMA
-    uint64_t *kv_empty = bars + kStages;        // [kStages] MMA -> TMA
-    uint64_t *q_full = bars + 2 * kStages;      // softmax threads -> MMA (both Q tiles written)
+    uint64_t *k_full = bars + 0;                // [kStages] TMA -> MMA
+    uint64_t *k_empty = bars + kStages;         // [kStages] MMA -> TMA
+    uint64_t *v_full = bars + 2 * kStages;      // [kStages] TMA -> MMA
+    uint64_t *v_empty = bars + 3 * kStages;     // [kStages] MMA -> TMA
+    uint64_t *q_full = bars + 4 * kStages;      // softmax threads -> MMA (both Q tiles written)
     uint64_t *s_full = q_full + 1;              // [kQT] MMA -> softmax (S ready, O holds all PVs before it)
     uint64_t *p_full = s_full + kQT;            // [kQT] softmax -> MMA (S read, P written, O rescaled)
     uint64_t *o_done = p_full + kQT;            // [kQT] MMA -> softmax (last PV finished)
     volatile uint32_t *tmem_holder = reinterpret_cast<volatile uint32_t *>(o_done + kQT);
-    static_assert((2 * kStages + 1 + 3 * kQT + 1) * 8 <= kSmemUsed - kOffBar, "barrier area");
+    static_assert((4 * kStages + 1 + 3 * kQT + 1) * 8 <= kSmemUsed - kOffBar, "barrier area");
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int kvh = blockIdx.y;
@@ -208,8 +213,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < kStages; ++i) {
-            mbar_init(&kv_full[i], 1);
-            mbar_init(&kv_empty[i], 1);
+            mbar_init(&k_full[i], 1);
+            mbar_init(&k_empty[i], 1);
+            mbar_init(&v_full[i], 1);
+            mbar_init(&v_empty[i], 1);
         }
         mbar_init(q_full, kQT * 128);
         for (int g = 0; g < kQT; ++g) {
@@ -242,32 +249,43 @@ __global__ void __launch_bounds__(kThreads, 1)
         auto chunk = [&](int c) { return c * 32 + lane < nent ? table[c * 32 + lane] : -1; };
         int ent_cur = chunk(0), ent_nxt = chunk(1);
         constexpr int kTilesPerChunk = 32 / kBlocksPerTile;
-        for (int j = 0; j < ntiles; ++j) {
-            const int st = j % kStages;
-            if (j > 0 && j % kTilesPerChunk == 0) {
-                ent_cur = ent_nxt;
-                ent_nxt = chunk(j / kTilesPerChunk + 1);
-            }
-            const int blk = __shfl_sync(0xffffffffu, ent_cur, (j % kTilesPerChunk) * kBlocksPerTile + (lane % kBlocksPerTile));
+        // row of block `lane` of tile j in the pool (zero-fill row when past kend)
+        auto tile_row = [&](int j, int blk) {
             int y = oob_row;
             if (lane < kBlocksPerTile && j * kNK + lane * BS <= kend) {
                 if (blk >= 0 && blk < p.num_blocks) y = (blk * p.num_kv_heads + kvh) * BS;
                 else flag_error(p.d_err, PA_DEVERR_BLOCK_RANGE);
             }
+            return y;
+        };
+        auto load = [&](const CUtensorMap *map, uint64_t *full, uint64_t *empty, uint32_t ring, int j, int y) {
+            const int st = j % kStages;
             if (lane == 0) {
-                if (j >= kStages) wait_or_flag(&kv_empty[st], (uint32_t)(j / kStages - 1) & 1u, p.d_err);
-                mbar_arrive_expect_tx(&kv_full[st], 2u * kKVTile);
+                if (j >= kStages) wait_or_flag(&empty[st], (uint32_t)(j / kStages - 1) & 1u, p.d_err);
+                mbar_arrive_expect_tx(&full[st], (uint32_t)kKVTile);
             }
             __syncwarp();
             if (lane < kBlocksPerTile) {
-                const uint32_t k_dst = sb + kOffKV + st * kStageBytes + lane * BS * 128;
-                const uint32_t v_dst = k_dst + kKVTile;
-                tma_2d(k_dst, &tmk, 0, y, &kv_full[st]);
-                tma_2d(k_dst + kKVHalf, &tmk, 64, y, &kv_full[st]);
-                tma_2d(v_dst, &tmv, 0, y, &kv_full[st]);
-                tma_2d(v_dst + kKVHalf, &tmv, 64, y, &kv_full[st]);
+                const uint32_t dst = ring + st * kKVTile + lane * BS * 128;
+                tma_2d(dst, map, 0, y, &full[st]);
+                tma_2d(dst + kKVHalf, map, 64, y, &full[st]);
             }
+        };
+        // order: K(0), then K(j) before V(j-1) -- both are first needed by the
+        // same MMA round, and K(j)'s slot frees up earlier
+        int y_prev = oob_row;
+        for (int j = 0; j < ntiles; ++j) {
+            if (j > 0 && j % kTilesPerChunk == 0) {
+                ent_cur = ent_nxt;
+                ent_nxt = chunk(j / kTilesPerChunk + 1);
+            }
+            const int blk = __shfl_sync(0xffffffffu, ent_cur, (j % kTilesPerChunk) * kBlocksPerTile + (lane % kBlocksPerTile));
+            const int y = tile_row(j, blk);
+            load(&tmk, k_full, k_empty, sb + kOffK, j, y);
+            if (j >= 1) load(&tmv, v_full, v_empty, sb + kOffV, j - 1, y_prev);
+            y_prev = y;
         }
+        load(&tmv, v_full, v_empty, sb + kOffV, ntiles - 1, y_prev);
     } else if (warp == 1) {
         // ============================================================ MMA issuer
         if (lane == 0) {
@@ -277,16 +295,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             // descriptor low words of Q tile 0 and of stage 0's K and V; the
             // rest are fixed offsets from these
             const uint32_t q_lo0 = desc_lo(sb + kOffQ, 16);
-            const uint32_t k_lo0 = desc_lo(sb + kOffKV, 16);
-            const uint32_t v_lo0 = desc_lo(sb + kOffKV + kKVTile, kKVHalf);
+            const uint32_t k_lo0 = desc_lo(sb + kOffK, 16);
+            const uint32_t v_lo0 = desc_lo(sb + kOffV, kKVHalf);
             wait_or_flag(q_full, 0, p.d_err);
             tc_fence_after();
             for (int j = 0; j <= ntiles; ++j) {
                 const int st = j % kStages, stp = (j + kStages - 1) % kStages;
-                if (j < ntiles) {
-                    wait_or_flag(&kv_full[st], (uint32_t)(j / kStages) & 1u, p.d_err);
-                    tc_fence_after();
-                }
+                if (j >= 1) wait_or_flag(&v_full[stp], (uint32_t)((j - 1) / kStages) & 1u, p.d_err);
 #pragma unroll
                 for (int g = 0; g < kQT; ++g) {
                     const uint32_t tS = tmem + kColS + g * kNK;
@@ -294,18 +309,23 @@ __global__ void __launch_bounds__(kThreads, 1)
                         // O_g += P_g(j-1) V(j-1); P sits in S_g's first 64 columns
                         wait_or_flag(&p_full[g], (uint32_t)(j - 1) & 1u, p.d_err);
                         tc_fence_after();
-                        const uint32_t v_lo = v_lo0 + stp * (kStageBytes >> 4);
+                        const uint32_t v_lo = v_lo0 + stp * (kKVTile >> 4);
 #pragma unroll
                         for (int kk = 0; kk < kNK / 16; ++kk)
                             mma_f16_ts(tmem + kColO + g * kD, tS + kk * 8, desc_of(v_lo + kk * (2048 >> 4), hi),
                                        idesc_pv, j > 1 || kk > 0);
                         if (j == ntiles) mma_commit(&o_done[g]);
-                        if (g == kQT - 1) mma_commit(&kv_empty[stp]);
+                        // release V(j-1)'s slot only if the producer will wait for it
+                        if (g == kQT - 1 && j - 1 + kStages < ntiles) mma_commit(&v_empty[stp]);
                     }
                     if (j < ntiles) {
+                        if (g == 0) {
+                            wait_or_flag(&k_full[st], (uint32_t)(j / kStages) & 1u, p.d_err);
+                            tc_fence_after();
+                        }
                         // S_g = Q_g K(j)^T
                         const uint32_t q_lo = q_lo0 + g * (kQTile >> 4);
-                        const uint32_t k_lo = k_lo0 + st * (kStageBytes >> 4);
+                        const uint32_t k_lo = k_lo0 + st * (kKVTile >> 4);
 #pragma unroll
                         for (int kk = 0; kk < 8; ++kk) {
                             const uint32_t qo = ((kk >> 2) * kQHalf + (kk & 3) * 32) >> 4;
@@ -313,6 +333,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                             mma_f16(tS, desc_of(q_lo + qo, hi), desc_of(k_lo + ko, hi), idesc_qk, kk > 0);
                         }
                         mma_commit(&s_full[g]);
+                        if (g == kQT - 1 && j + kStages < ntiles) mma_commit(&k_empty[st]);
                     }
                 }
             }
@@ -445,9 +466,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // V rows past the last key any row sees hold whatever the pool
                 // has there (possibly NaN, and 0 * NaN poisons O): zero them
                 const int st_kv = j % kStages;
-                wait_or_flag(&kv_full[st_kv], (uint32_t)(j / kStages) & 1u, p.d_err);
+                wait_or_flag(&v_full[st_kv], (uint32_t)(j / kStages) & 1u, p.d_err);
                 const int z0 = kend + 1 - kb;
-                const uint32_t v_s = sb + kOffKV + st_kv * kStageBytes + kKVTile;
+                const uint32_t v_s = sb + kOffV + st_kv * kKVTile;
                 for (int idx = t; idx < (kNK - z0) * 16; idx += 128) {
                     const int r = z0 + (idx >> 4), h = (idx >> 3) & 1, c = idx & 7;
                     asm volatile("st.shared.v4.u32 [%0], {%1,%1,%1,%1};" ::"r"(v_s + h * kKVHalf + r * 128 + c * 16),
