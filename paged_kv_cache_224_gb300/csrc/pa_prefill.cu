@@ -8,7 +8,11 @@
 //
 // One CTA computes two tiles of 128 query rows -- 256/G chunk positions times
 // the G query heads of one kv head -- against 128-key tiles that both Q tiles
-// share (each K/V byte brought into shared memory serves 256 rows):
+// share (each K/V byte brought into shared memory serves 256 rows).  CTAs run
+// in clusters of two on adjacent row ranges of the same kv head, and each
+// K/V tile is fetched once for the pair: each CTA copies half of the tile's
+// blocks and multicasts them into both CTAs' shared memory (the TMA unit's
+// cost is per copy, and with 16-row blocks the copies are small).
 //   warp 0    TMA producer: for each key tile, one 2-D tensor copy per
 //             (block, 64-dim half) of K and of V, straight from the paged pool
 //             into a 128-byte-swizzled shared layout.  K and V have rings of
@@ -59,6 +63,8 @@ constexpr int kOffBar = kOffV + kStages * kKVTile;         // 192 KB
 constexpr int kSmemUsed = kOffBar + 256;
 constexpr int kSmemAlloc = kSmemUsed + 1024;               // room to align the base to 1 KB
 constexpr int kThreads = 64 + kQT * 128;
+constexpr int kCluster = 2;                    // CTAs sharing each K/V tile
+constexpr uint16_t kClusterMask = (1u << kCluster) - 1;
 // TMEM columns: S of each Q tile (128 fp32; P overwrites its first 64 columns
 // as 128 packed pairs), O of each Q tile (128 fp32)
 constexpr uint32_t kColS = 0, kColO = 256;
@@ -160,12 +166,36 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const float (&v)[32]) 
 __device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 __device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
-__device__ __forceinline__ void tma_2d(uint32_t dst, const CUtensorMap *map, int x, int y, uint64_t *bar) {
+// 2-D tensor copy global -> shared, written to the same offset in every CTA
+// of the cluster named in cta_mask, completing bytes on the barrier at the
+// same offset in each.
+__device__ __forceinline__ void tma_2d_mc(uint32_t dst, const CUtensorMap *map, int x, int y, uint64_t *bar,
+                                          uint16_t cta_mask) {
     asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], "
-        "[%4];" ::"r"(dst),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_addr(bar))
+        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.multicast::cluster"
+        " [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_addr(bar)), "h"(cta_mask)
         : "memory");
+}
+
+// Arrive (once) on the barrier at this offset in every CTA of cta_mask when
+// all MMAs issued so far by this thread have completed.
+__device__ __forceinline__ void mma_commit_mc(uint64_t *bar, uint16_t cta_mask) {
+    asm volatile(
+        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
+            smem_addr(bar)),
+        "h"(cta_mask)
+        : "memory");
+}
+
+__device__ __forceinline__ uint32_t cluster_rank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+
+__device__ __forceinline__ void cluster_sync() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 
 __device__ __forceinline__ void mbar_arrive1(uint64_t *bar) {
@@ -185,6 +215,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     constexpr bool kBf16 = std::is_same<T, __nv_bfloat16>::value;
     constexpr int kBlocksPerTile = kNK / BS;
     static_assert(kNK % BS == 0 && kBlocksPerTile <= 32 && 32 % kBlocksPerTile == 0, "block_size");
+    static_assert(kBlocksPerTile % kCluster == 0, "each CTA of a cluster copies the same number of blocks");
     static_assert(kM % G == 0, "group");
 
     extern __shared__ unsigned char smem_raw[];
@@ -205,18 +236,22 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int kvh = blockIdx.y;
+    const int rank = (int)cluster_rank();
     const int row0 = blockIdx.x * (kQT * kM);
     const int nrows = p.chunk_len * G;
-    const int i_last = min(p.chunk_len - 1, (row0 + kQT * kM - 1) / G);
-    const int kend = p.prefix_len + i_last;  // last key any row of this CTA sees
+    // both CTAs of a cluster walk the same key tiles: up to the last key any
+    // row of the cluster sees
+    const int cl_row_end = (blockIdx.x - rank + kCluster) * (kQT * kM);
+    const int i_last = min(p.chunk_len - 1, (cl_row_end - 1) / G);
+    const int kend = p.prefix_len + i_last;
     const int ntiles = kend / kNK + 1;
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < kStages; ++i) {
             mbar_init(&k_full[i], 1);
-            mbar_init(&k_empty[i], 1);
+            mbar_init(&k_empty[i], kCluster);  // released by the MMA issuer of each CTA
             mbar_init(&v_full[i], 1);
-            mbar_init(&v_empty[i], 1);
+            mbar_init(&v_empty[i], kCluster);
         }
         mbar_init(q_full, kQT * 128);
         for (int g = 0; g < kQT; ++g) {
@@ -235,6 +270,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     tc_fence_before();
     __syncthreads();
+    cluster_sync();  // the peer's copies and releases may target these barriers from here on
     tc_fence_after();
     const uint32_t tmem = *tmem_holder;
 
@@ -265,10 +301,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                 mbar_arrive_expect_tx(&full[st], (uint32_t)kKVTile);
             }
             __syncwarp();
-            if (lane < kBlocksPerTile) {
+            if (lane < kBlocksPerTile && lane % kCluster == rank) {
                 const uint32_t dst = ring + st * kKVTile + lane * BS * 128;
-                tma_2d(dst, map, 0, y, &full[st]);
-                tma_2d(dst + kKVHalf, map, 64, y, &full[st]);
+                tma_2d_mc(dst, map, 0, y, &full[st], kClusterMask);
+                tma_2d_mc(dst + kKVHalf, map, 64, y, &full[st], kClusterMask);
             }
         };
         // order: K(0), then K(j) before V(j-1) -- both are first needed by the
@@ -316,7 +352,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                                        idesc_pv, j > 1 || kk > 0);
                         if (j == ntiles) mma_commit(&o_done[g]);
                         // release V(j-1)'s slot only if the producer will wait for it
-                        if (g == kQT - 1 && j - 1 + kStages < ntiles) mma_commit(&v_empty[stp]);
+                        if (g == kQT - 1 && j - 1 + kStages < ntiles) mma_commit_mc(&v_empty[stp], kClusterMask);
                     }
                     if (j < ntiles) {
                         if (g == 0) {
@@ -333,7 +369,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                             mma_f16(tS, desc_of(q_lo + qo, hi), desc_of(k_lo + ko, hi), idesc_qk, kk > 0);
                         }
                         mma_commit(&s_full[g]);
-                        if (g == kQT - 1 && j + kStages < ntiles) mma_commit(&k_empty[st]);
+                        if (g == kQT - 1 && j + kStages < ntiles) mma_commit_mc(&k_empty[st], kClusterMask);
                     }
                 }
             }
@@ -507,6 +543,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     tc_fence_before();
     __syncthreads();
+    cluster_sync();  // neither CTA leaves while the other may still copy into it
     if (warp == 1) {
         tc_fence_after();
         asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols)
@@ -563,9 +600,20 @@ int launch_tc_t(const PrefillParams &p, cudaStream_t stream) {
     CUtensorMap tmk, tmv;
     if (!make_pool_map(&tmk, p.k_cache, p, BS, bf16) || !make_pool_map(&tmv, p.v_cache, p, BS, bf16))
         return PA_ERR_CUDA;
-    dim3 grid((p.chunk_len * G + kQT * kM - 1) / (kQT * kM), p.num_kv_heads);
-    kern<<<grid, kThreads, kSmemAlloc, stream>>>(p, tmk, tmv);
-    return cudaPeekAtLastError() == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+    const int tiles = (p.chunk_len * G + kQT * kM - 1) / (kQT * kM);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((tiles + kCluster - 1) / kCluster * kCluster, p.num_kv_heads);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = kSmemAlloc;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = kCluster;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, p, tmk, tmv) == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }
 
 template <typename T>
