@@ -46,14 +46,14 @@ def load_peaks():
     return FALLBACK_HBM_GBS, "fallback"
 
 
-def load_traffic(kernel_key: str):
-    """Per-launch DRAM bytes of the decode kernel from the committed ncu
-    summary, if it was taken on the current kernel source."""
+def load_traffic(kernel_key: str, source: str = "pa_decode.cuh"):
+    """Per-launch DRAM bytes of a kernel from the committed ncu summary, if
+    it was taken on the current kernel source."""
     path = os.path.join(ROOT, "profiles", "traffic.txt")
     if not os.path.exists(path):
         return None
     import hashlib
-    src = os.path.join(ROOT, "paged_kv_cache_224_gb300", "csrc", "pa_decode.cuh")
+    src = os.path.join(ROOT, "paged_kv_cache_224_gb300", "csrc", source)
     sha = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
     for line in open(path):
         parts = line.split()
@@ -276,8 +276,9 @@ def run_prefill_bench(args, world, rank, local, dev, stream):
                            "step": "pa_reshape_and_cache (chunk K/V) + pa_prefill_chunk",
                            "l2": "KV of one kv head (4.5 MB) is reused from L2 by its row tiles"},
                 "roofline": {"bound": "tensor", "achieved": round(achieved, 2), "peak": peak,
-                             "unit": "TFLOP/s", "frac": round(achieved / peak, 4), "traffic": None,
-                             "kernel": "prefill_kernel", "flops_per_launch": flops, "avg_ms": round(pf_ms, 5),
+                             "unit": "TFLOP/s", "frac": round(achieved / peak, 4),
+                             "traffic": load_traffic(case.name, "pa_prefill.cu"),
+                             "kernel": "prefill_tc_kernel", "flops_per_launch": flops, "avg_ms": round(pf_ms, 5),
                              "peak_kind": f"{kind} (bf16 dense, burst)"},
                 "gpu_launches": 2 * args.steps, "clocks": clk.summary()}
         print(json.dumps(line), flush=True)
