@@ -407,9 +407,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
 
         float m_run = -INFINITY;  // running max in scaled log2 units
-        float l8[8];
+        float2 l2[4];             // row sum as four pairs of partial sums
 #pragma unroll
-        for (int e = 0; e < 8; ++e) l8[e] = 0.f;
+        for (int e = 0; e < 4; ++e) l2[e] = make_float2(0.f, 0.f);
         for (int j = 0; j < ntiles; ++j) {
             wait_or_flag(&s_full[g], (uint32_t)j & 1u, p.d_err);
             tc_fence_after();
@@ -457,14 +457,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                         tmem_st32(tO + c * 32, v);
                     }
 #pragma unroll
-                    for (int e = 0; e < 8; ++e) l8[e] *= alpha;
+                    for (int e = 0; e < 4; ++e) l2[e] = __fmul2_rn(l2[e], make_float2(alpha, alpha));
                 }
                 m_run = mx;
             }
             // pass 2: P row t = 2^(s*scale - max), rounded to the input type,
             // packed over S's first 64 columns (half h goes to columns 32h..32h+31,
             // which pass 2 of half h-1 has already read)
-            const float neg_m = -m_run;
+            const float2 csc2 = make_float2(csc, csc), negm2 = make_float2(-m_run, -m_run);
 #pragma unroll 1
             for (int h = 0; h < 2; ++h) {
                 float s0[32], s1[32];
@@ -481,20 +481,14 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                     for (int c = 0; c < 64; ++c) s[c] = (kb + h * 64 + c <= plim) ? s[c] : -INFINITY;
                 }
+                // exponent arguments and row sums in packed fp32x2 arithmetic
                 uint32_t pk[32];
 #pragma unroll
-                for (int c = 0; c < 8; ++c) {
-                    float pr[8];
-#pragma unroll
-                    for (int e = 0; e < 8; ++e) {
-                        pr[e] = fast_exp2(fmaf(s[c * 8 + e], csc, neg_m));
-                        l8[e] += pr[e];
-                    }
-                    const uint4 u = pack8<T>(pr);
-                    pk[c * 4 + 0] = u.x;
-                    pk[c * 4 + 1] = u.y;
-                    pk[c * 4 + 2] = u.z;
-                    pk[c * 4 + 3] = u.w;
+                for (int c = 0; c < 32; ++c) {
+                    const float2 a = __ffma2_rn(make_float2(s[2 * c], s[2 * c + 1]), csc2, negm2);
+                    const float2 q = make_float2(fast_exp2(a.x), fast_exp2(a.y));
+                    l2[c & 3] = __fadd2_rn(l2[c & 3], q);
+                    pk[c] = Elem<T>::pack2(q.x, q.y);
                 }
                 tmem_st32u(tS + h * 32, pk);
             }
@@ -521,7 +515,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // epilogue: O row / l, rounded once, stored
         wait_or_flag(&o_done[g], 0, p.d_err);
         tc_fence_after();
-        const float l_run = ((l8[0] + l8[1]) + (l8[2] + l8[3])) + ((l8[4] + l8[5]) + (l8[6] + l8[7]));
+        const float l_run = ((l2[0].x + l2[0].y) + (l2[1].x + l2[1].y)) + ((l2[2].x + l2[2].y) + (l2[3].x + l2[3].y));
         const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
         T *orow = static_cast<T *>(p.out) + ((size_t)ipos * p.num_heads + kvh * G + head) * kD;
 #pragma unroll
