@@ -159,7 +159,7 @@ def make_case(name: str, seed_offset: int):
         return wl.long_context_case(block_size=16, seed=1004 + seed_offset)
     if name == "long_context_bs32":
         return wl.long_context_case(block_size=32, seed=1004 + seed_offset)
-    if name == "shared_prefix":
+    if name in ("shared_prefix", "shared_prefix_grouped"):
         return wl.shared_prefix_case(seed=1003 + seed_offset)
     raise SystemExit(f"unknown workload {name}")
 
@@ -291,7 +291,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="llama_gqa", choices=["llama_gqa", "opt13b_mha", "long_context", "long_context_bs32",
-                             "shared_prefix", "chunked_prefill"])
+                             "shared_prefix", "shared_prefix_grouped", "chunked_prefill"])
     ap.add_argument("--partition-tokens", type=int, default=0)
     ap.add_argument("--e2e-steps", type=int, default=50)
     ap.add_argument("--cpu-seqs", type=int, default=64, help="sequences in the CPU-baseline sample")
@@ -337,13 +337,31 @@ def main():
     lens = torch.as_tensor(case.context_lens, device=dev)
     out = torch.empty_like(t["query"])
     pt = args.partition_tokens
-    ws = pa.decode_workspace(t["query"], case.block_size, case.max_context_len, pt)
+    # shared_prefix_grouped: the same workload, decoded with the shared-prefix
+    # entry point (each group's prefix blocks read once)
+    grouped = args.workload == "shared_prefix_grouped"
+    if grouped:
+        n = pa.pa_decode_shared_prefix_workspace_bytes(case.num_seqs, case.num_heads, case.head_dim,
+                                                       case.block_size, case.max_context_len,
+                                                       case.shared_blocks, pt)
+        ws = torch.empty(max(n, 1), dtype=torch.uint8, device=dev)
+    else:
+        ws = pa.decode_workspace(t["query"], case.block_size, case.max_context_len, pt)
     err = torch.zeros(1, dtype=torch.int32, device=dev)
     part = pa.pa_decode_partition_tokens(case.num_seqs, case.num_kv_heads, case.block_size,
                                          case.max_context_len, pt)
     max_parts = -(-case.max_context_len // part)
     pairs = torch.as_tensor(case.cow_pairs, device=dev) if case.cow_pairs.shape[0] else None
-    launches_per_step = (1 if pairs is not None else 0) + 1 + 1 + (1 if max_parts > 1 else 0)
+    launches_per_step = (1 if pairs is not None else 0) + 1 + (3 if grouped else 1 + (1 if max_parts > 1 else 0))
+
+    def decode(q, bt_, lens_):
+        if grouped:
+            pa.pa_decode_shared_prefix(out, q, t["k_cache"], t["v_cache"], bt_, lens_, case.scale,
+                                       case.max_context_len, case.group_size, case.shared_blocks,
+                                       partition_tokens=pt, workspace=ws, d_err=err)
+        else:
+            pa.pa_decode(out, q, t["k_cache"], t["v_cache"], bt_, lens_, case.scale,
+                         case.max_context_len, partition_tokens=pt, workspace=ws, d_err=err)
 
     def cow():
         # copy-on-write of shared blocks before the tails are written (idempotent across steps)
@@ -353,8 +371,7 @@ def main():
     def step():
         cow()
         pa.pa_reshape_and_cache(t["new_key"], t["new_value"], t["k_cache"], t["v_cache"], slots, d_err=err)
-        pa.pa_decode(out, t["query"], t["k_cache"], t["v_cache"], bt, lens, case.scale,
-                     case.max_context_len, partition_tokens=pt, workspace=ws, d_err=err)
+        decode(t["query"], bt, lens)
 
     for _ in range(args.warmup):
         step()
@@ -375,8 +392,7 @@ def main():
             cow()
             pa.pa_reshape_and_cache(t["new_key"], t["new_value"], t["k_cache"], t["v_cache"], slots, d_err=err)
             ev[i][0].record(stream)
-            pa.pa_decode(out, t["query"], t["k_cache"], t["v_cache"], bt, lens, case.scale,
-                         case.max_context_len, partition_tokens=pt, workspace=ws, d_err=err)
+            decode(t["query"], bt, lens)
             ev[i][1].record(stream)
         stop.record(stream)
         torch.cuda.synchronize()
@@ -415,8 +431,7 @@ def main():
             d.copy_(h, non_blocking=True)
         cow()
         pa.pa_reshape_and_cache(d_nk, d_nv, t["k_cache"], t["v_cache"], d_slots, d_err=err)
-        pa.pa_decode(out, d_q, t["k_cache"], t["v_cache"], d_bt, d_lens, case.scale,
-                     case.max_context_len, partition_tokens=pt, workspace=ws, d_err=err)
+        decode(d_q, d_bt, d_lens)
         h_out.copy_(out, non_blocking=True)
 
     for _ in range(3):
@@ -451,14 +466,18 @@ def main():
                            2 * case.num_blocks * case.num_kv_heads * case.block_size * case.head_dim * 2 / 1e9,
                            case.kv_bytes() / 1e9),
                        "step": ("pa_copy_blocks + " if pairs is not None else "")
-                               + f"pa_reshape_and_cache ({case.num_new_tokens} tokens) + pa_decode",
+                               + f"pa_reshape_and_cache ({case.num_new_tokens} tokens) + "
+                               + ("pa_decode_shared_prefix (groups of %d, %d shared blocks)" % (
+                                   case.group_size, case.shared_blocks) if grouped else "pa_decode"),
+                       "unique_kv_bytes": case.unique_kv_bytes(),
                        "parallelism": f"replicas x{world}, sequences sharded, no collective"},
             "pct_of_peak": round(100 * gbs / peak, 2),
             "tokens_per_s": round(tokens_per_s, 1),
             "context_tokens_per_s": round(float(case.context_lens.sum()) * world / (ms_per_step / 1e3), 1),
             "roofline": {"bound": "hbm", "achieved": round(dec_achieved, 2), "peak": peak,
                          "unit": "GB/s", "frac": round(dec_achieved / peak, 4), "traffic": traffic,
-                         "kernel": "pa_decode (decode_kernel + decode_reduce_kernel)",
+                         "kernel": "pa_decode_shared_prefix (decode_kernel x2 + decode_reduce_kernel)"
+                                   if grouped else "pa_decode (decode_kernel + decode_reduce_kernel)",
                          "bytes_per_launch": case.decode_bytes(), "avg_ms": round(dec_avg_ms, 5),
                          "peak_kind": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured" else "fallback"},
             "e2e": {"value": round(e2e_gbs, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d,

@@ -72,6 +72,7 @@ typedef enum {
 #define PA_DEVERR_CONTEXT_RANGE 0x4 /* context length < 0, > max_context_len or > table */
 #define PA_DEVERR_COPY_PAIR 0x8     /* copy pair out of pool, src==dst, or dst conflict */
 #define PA_DEVERR_TIMEOUT 0x10      /* a bounded pipeline wait gave up */
+#define PA_DEVERR_PREFIX 0x20       /* pa_decode_shared_prefix: a group's prefix table rows differ */
 
 /* Human-readable name of a pa_status value. */
 PA_API const char *pa_status_string(int status);
@@ -144,6 +145,42 @@ PA_API int pa_decode(void *out, const void *query, const void *k_cache, const vo
               int num_blocks, int max_context_len, float scale, int partition_tokens,
               pa_dtype dtype, void *workspace, size_t workspace_bytes, int *d_err,
               void *stream);
+
+/*
+ * pa_decode_shared_prefix -- pa_decode for batches in which consecutive
+ * groups of sequences share the physical blocks of a common prefix (several
+ * samples of one prompt; the pages' parallel sampling / shared-prefix case:
+ * "vLLM PagedAttention chuyen sau" (locionic.com), "Co che APC", and "vLLM"
+ * (tellworld.net), "PagedAttention").  Each shared block is read from memory
+ * once per group instead of once per sequence.
+ *
+ * Same arguments, layout, results and errors as pa_decode, plus:
+ *   group_size     sequences g*group_size .. g*group_size+group_size-1 form
+ *                  group g; num_seqs % group_size == 0, and group_size times
+ *                  num_heads/num_kv_heads must be 1, 2, 4 or 8
+ *   prefix_blocks  >= 1: the first prefix_blocks entries of every block-table
+ *                  row of a group are the same physical blocks, and every
+ *                  sequence's context covers them (context_lens[s] >=
+ *                  prefix_blocks*block_size).  A group whose rows differ there
+ *                  sets PA_DEVERR_PREFIX (its outputs are then undefined); a
+ *                  context shorter than the prefix sets PA_DEVERR_CONTEXT_RANGE.
+ *   workspace      always required: pa_decode_shared_prefix_workspace_bytes().
+ * The output equals pa_decode's within the attention tolerance (the same
+ * softmax, merged from partials of the prefix and of each sequence's own
+ * tokens; not bit-identical to pa_decode).  Internally: one pass attends each
+ * group's queries over its shared blocks as one head group, one pass attends
+ * each sequence over its own tokens, and a log-sum-exp merge combines them.
+ */
+PA_API size_t pa_decode_shared_prefix_workspace_bytes(int num_seqs, int num_heads, int head_dim,
+                                                      int block_size, int max_context_len,
+                                                      int prefix_blocks, int partition_tokens);
+PA_API int pa_decode_shared_prefix(void *out, const void *query, const void *k_cache,
+                                   const void *v_cache, const int32_t *block_tables,
+                                   int max_blocks_per_seq, const int32_t *context_lens, int num_seqs,
+                                   int group_size, int prefix_blocks, int num_heads, int num_kv_heads,
+                                   int head_dim, int block_size, int num_blocks, int max_context_len,
+                                   float scale, int partition_tokens, pa_dtype dtype, void *workspace,
+                                   size_t workspace_bytes, int *d_err, void *stream);
 
 /*
  * pa_decode_noalloc -- pa_decode for callers that must not allocate device

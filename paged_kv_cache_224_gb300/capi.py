@@ -23,7 +23,7 @@ DEVERR = {"slot_range": 0x1, "block_range": 0x2, "context_range": 0x4, "copy_pai
           "timeout": 0x10}
 EXPORTED = ("pa_status_string", "pa_reshape_and_cache", "pa_decode_partition_tokens",
             "pa_decode_workspace_bytes", "pa_decode", "pa_copy_blocks", "pa_prefill_chunk",
-            "pa_decode_noalloc")
+            "pa_decode_noalloc", "pa_decode_shared_prefix_workspace_bytes", "pa_decode_shared_prefix")
 PA_ERR_SCRATCH_LIMIT = -7
 NOALLOC_SCRATCH_BYTES = 64 << 20
 
@@ -59,6 +59,11 @@ def lib() -> ctypes.CDLL:
         L.pa_decode_noalloc.argtypes = [p, p, p, p, p, i, p, i, i, i, i, i, i, i, ctypes.c_float,
                                         i, i, p, p]
         L.pa_decode_noalloc.restype = i
+        L.pa_decode_shared_prefix_workspace_bytes.argtypes = [i, i, i, i, i, i, i]
+        L.pa_decode_shared_prefix_workspace_bytes.restype = sz
+        L.pa_decode_shared_prefix.argtypes = [p, p, p, p, p, i, p, i, i, i, i, i, i, i, i, i,
+                                              ctypes.c_float, i, i, p, sz, p, p]
+        L.pa_decode_shared_prefix.restype = i
         L.pa_copy_blocks.argtypes = [p, p, p, i, i, i, i, i, i, p, p]
         L.pa_copy_blocks.restype = i
         L.pa_prefill_chunk.argtypes = [p, p, p, p, p, i, i, i, i, i, i, i, ctypes.c_float, i, p, p]
@@ -159,6 +164,38 @@ def pa_decode(out, query, k_cache, v_cache, block_tables, context_lens, scale, m
                          _ptr(workspace), workspace.numel() * workspace.element_size(),
                          _ptr(d_err), _stream(query, stream))
     _check("pa_decode", rc)
+
+
+def pa_decode_shared_prefix_workspace_bytes(num_seqs, num_heads, head_dim, block_size,
+                                            max_context_len, prefix_blocks, partition_tokens=0) -> int:
+    return lib().pa_decode_shared_prefix_workspace_bytes(num_seqs, num_heads, head_dim, block_size,
+                                                         max_context_len, prefix_blocks, partition_tokens)
+
+
+def pa_decode_shared_prefix(out, query, k_cache, v_cache, block_tables, context_lens, scale,
+                            max_context_len, group_size, prefix_blocks, partition_tokens=0,
+                            workspace=None, d_err=None, stream=None):
+    """``pa_decode`` for batches whose consecutive groups of ``group_size``
+    sequences share their first ``prefix_blocks`` physical blocks."""
+    _dev(out, query, k_cache, v_cache, block_tables, context_lens, workspace, d_err)
+    if block_tables.dtype != torch.int32 or context_lens.dtype != torch.int32:
+        raise TypeError("block_tables and context_lens must be int32")
+    NB, Hkv, bs, D = k_cache.shape
+    B, Hq, Dq = query.shape
+    if Dq != D or out.shape != query.shape or block_tables.shape[0] != B or context_lens.shape != (B,):
+        raise ValueError("shape mismatch")
+    if not (out.dtype == query.dtype == k_cache.dtype == v_cache.dtype):
+        raise TypeError("dtype mismatch")
+    if workspace is None:
+        n = pa_decode_shared_prefix_workspace_bytes(B, Hq, D, bs, max_context_len, prefix_blocks,
+                                                    partition_tokens)
+        workspace = torch.empty(max(n, 1), dtype=torch.uint8, device=query.device)
+    rc = lib().pa_decode_shared_prefix(
+        _ptr(out), _ptr(query), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables), block_tables.shape[1],
+        _ptr(context_lens), B, int(group_size), int(prefix_blocks), Hq, Hkv, D, bs, NB,
+        int(max_context_len), float(scale), int(partition_tokens), _dt(query), _ptr(workspace),
+        workspace.numel() * workspace.element_size(), _ptr(d_err), _stream(query, stream))
+    _check("pa_decode_shared_prefix", rc)
 
 
 def pa_decode_noalloc(out, query, k_cache, v_cache, block_tables, context_lens, scale,

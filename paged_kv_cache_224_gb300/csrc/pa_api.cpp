@@ -3,6 +3,7 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <algorithm>
 #include <cmath>
 
 #include "../../include/pa.h"
@@ -14,10 +15,18 @@ int launch_decode_bf16(int head_dim, int block_size, int group, const DecodePara
 int launch_decode_f16(int head_dim, int block_size, int group, const DecodeParams &p,
                       cudaStream_t stream);
 
+int launch_decode_reduce_bf16(int head_dim, const DecodeParams &p, cudaStream_t stream);
+int launch_decode_reduce_f16(int head_dim, const DecodeParams &p, cudaStream_t stream);
+
 int launch_decode(pa_dtype dt, int head_dim, int block_size, int group, const DecodeParams &p,
                   cudaStream_t stream) {
     return dt == PA_BF16 ? launch_decode_bf16(head_dim, block_size, group, p, stream)
                          : launch_decode_f16(head_dim, block_size, group, p, stream);
+}
+
+int launch_decode_reduce(pa_dtype dt, int head_dim, const DecodeParams &p, cudaStream_t stream) {
+    return dt == PA_BF16 ? launch_decode_reduce_bf16(head_dim, p, stream)
+                         : launch_decode_reduce_f16(head_dim, p, stream);
 }
 
 // Default split: 512-token partitions.  A sequence that fits one partition
@@ -153,6 +162,10 @@ int pa_decode(void *out, const void *query, const void *k_cache, const void *v_c
     p.partition_tokens = pt;
     p.max_partitions = mp;
     p.scale_log2 = scale * 1.4426950408889634f;
+    p.grp_size = 1;
+    p.grp_inner = group;
+    p.table_stride = max_blocks_per_seq;
+    p.slots = mp;
     if (mp > 1) {
         const size_t need = pa_decode_workspace_bytes(num_seqs, num_heads, head_dim, block_size,
                                                       max_context_len, pt);
@@ -165,6 +178,107 @@ int pa_decode(void *out, const void *query, const void *k_cache, const void *v_c
     }
     return pa::launch_decode(dtype, head_dim, block_size, group, p,
                              static_cast<cudaStream_t>(stream));
+}
+
+size_t pa_decode_shared_prefix_workspace_bytes(int num_seqs, int num_heads, int head_dim,
+                                                int block_size, int max_context_len, int prefix_blocks,
+                                                int partition_tokens) {
+    if (num_seqs <= 0 || num_heads <= 0 || head_dim <= 0 || block_size <= 0 || max_context_len < 0 ||
+        prefix_blocks <= 0)
+        return 0;
+    const int pt = resolve_partition(num_seqs, 1, block_size, max_context_len, partition_tokens);
+    if (pt <= 0) return 0;
+    const int prefix_tokens = prefix_blocks * block_size;
+    const int slots = max_parts(prefix_tokens, pt) + max_parts(std::max(max_context_len - prefix_tokens, 0), pt);
+    const size_t n = (size_t)num_seqs * num_heads * slots;
+    const size_t acc = (n * head_dim * sizeof(float) + 255) / 256 * 256;
+    return acc + n * 2 * sizeof(float);
+}
+
+int pa_decode_shared_prefix(void *out, const void *query, const void *k_cache, const void *v_cache,
+                            const int32_t *block_tables, int max_blocks_per_seq, const int32_t *context_lens,
+                            int num_seqs, int group_size, int prefix_blocks, int num_heads, int num_kv_heads,
+                            int head_dim, int block_size, int num_blocks, int max_context_len, float scale,
+                            int partition_tokens, pa_dtype dtype, void *workspace, size_t workspace_bytes,
+                            int *d_err, void *stream) {
+    if (num_seqs < 0 || num_heads <= 0 || num_kv_heads <= 0 || head_dim <= 0 || block_size <= 0 ||
+        num_blocks <= 0 || max_blocks_per_seq <= 0 || max_context_len < 0 || !good_dtype(dtype) ||
+        group_size <= 0 || prefix_blocks <= 0)
+        return PA_ERR_INVALID_ARG;
+    if (num_heads % num_kv_heads || num_seqs % group_size) return PA_ERR_INVALID_ARG;
+    if (prefix_blocks > max_blocks_per_seq || (long long)prefix_blocks * block_size > max_context_len)
+        return PA_ERR_OUT_OF_RANGE;
+    if (!std::isfinite(scale)) return PA_ERR_OUT_OF_RANGE;
+    if (num_seqs == 0) return PA_OK;
+    if (!out || !query || !k_cache || !v_cache || !block_tables || !context_lens) return PA_ERR_INVALID_ARG;
+    const int group = num_heads / num_kv_heads;
+    const long long vgroup = (long long)group * group_size;  // heads per kv head in the prefix pass
+    if (!decode_shape_supported(head_dim, block_size, group) || vgroup > 8 ||
+        !decode_shape_supported(head_dim, block_size, (int)vgroup))
+        return PA_ERR_UNSUPPORTED;
+    if (!aligned16(out) || !aligned16(query) || !aligned16(k_cache) || !aligned16(v_cache))
+        return PA_ERR_ALIGNMENT;
+    const int pt = resolve_partition(num_seqs, num_kv_heads, block_size, max_context_len, partition_tokens);
+    if (pt <= 0) return PA_ERR_OUT_OF_RANGE;
+    const int prefix_tokens = prefix_blocks * block_size;
+    const int p_pre = max_parts(prefix_tokens, pt);
+    const int p_tail = max_parts(std::max(max_context_len - prefix_tokens, 0), pt);
+    const size_t need = pa_decode_shared_prefix_workspace_bytes(num_seqs, num_heads, head_dim, block_size,
+                                                                max_context_len, prefix_blocks, pt);
+    if (!workspace || workspace_bytes < need) return PA_ERR_WORKSPACE;
+    if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return PA_ERR_ALIGNMENT;
+    const size_t n = (size_t)num_seqs * num_heads * (p_pre + p_tail);
+    const size_t acc = (n * head_dim * sizeof(float) + 255) / 256 * 256;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+
+    pa::DecodeParams p{};
+    p.out = out;
+    p.query = query;
+    p.k_cache = k_cache;
+    p.v_cache = v_cache;
+    p.block_tables = block_tables;
+    p.context_lens = context_lens;
+    p.d_err = d_err;
+    p.num_heads = num_heads;
+    p.num_kv_heads = num_kv_heads;
+    p.max_blocks_per_seq = max_blocks_per_seq;
+    p.num_blocks = num_blocks;
+    p.max_context_len = max_context_len;
+    p.block_size = block_size;
+    p.partition_tokens = pt;
+    p.scale_log2 = scale * 1.4426950408889634f;
+    p.ws_acc = static_cast<float *>(workspace);
+    p.ws_ml = reinterpret_cast<float2 *>(static_cast<char *>(workspace) + acc);
+    p.slots = p_pre + p_tail;
+    p.force_partials = 1;
+
+    // pass 1: each group's queries over its shared blocks, one head group per kv head
+    pa::DecodeParams pre = p;
+    pre.num_seqs = num_seqs / group_size;
+    pre.grp_size = group_size;
+    pre.grp_inner = group;
+    pre.table_stride = group_size * max_blocks_per_seq;
+    pre.len_fixed = prefix_tokens;
+    pre.max_partitions = p_pre;
+    int rc = pa::launch_decode(dtype, head_dim, block_size, (int)vgroup, pre, st);
+    if (rc != PA_OK) return rc;
+
+    // pass 2: every sequence over its own tokens after the prefix
+    pa::DecodeParams tail = p;
+    tail.num_seqs = num_seqs;
+    tail.grp_size = 1;
+    tail.grp_inner = group;
+    tail.table_stride = max_blocks_per_seq;
+    tail.len_offset = prefix_tokens;
+    tail.part_base = p_pre;
+    tail.max_partitions = p_tail;
+    rc = pa::launch_decode(dtype, head_dim, block_size, group, tail, st);
+    if (rc != PA_OK) return rc;
+
+    // merge: p_pre prefix slots plus one per partition of the sequence's own tokens
+    pa::DecodeParams red = tail;
+    red.red_fixed_slots = p_pre;
+    return pa::launch_decode_reduce(dtype, head_dim, red, st);
 }
 
 int pa_copy_blocks(void *k_cache, void *v_cache, const int64_t *pairs, int num_pairs,

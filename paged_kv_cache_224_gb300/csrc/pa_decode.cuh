@@ -268,11 +268,26 @@ __global__ void __launch_bounds__(NW * 32, decode_min_ctas<G>()) decode_kernel(c
     const int s = rem / p.num_kv_heads;
     const int kvh = rem - s * p.num_kv_heads;
 
-    int L = p.context_lens[s];
-    const int Lcap = min(p.max_context_len, p.max_blocks_per_seq * BS);
-    if (L < 0 || L > Lcap) {
-        if (threadIdx.x == 0 && part == 0 && kvh == 0) flag_error(p.d_err, PA_DEVERR_CONTEXT_RANGE);
-        L = L < 0 ? 0 : Lcap;
+    int L;
+    if (p.len_fixed > 0) {
+        L = p.len_fixed;
+    } else {
+        L = p.context_lens[s] - p.len_offset;
+        const int Lcap = min(p.max_context_len, p.max_blocks_per_seq * BS) - p.len_offset;
+        if (L < 0 || L > Lcap) {
+            if (threadIdx.x == 0 && part == 0 && kvh == 0) flag_error(p.d_err, PA_DEVERR_CONTEXT_RANGE);
+            L = L < 0 ? 0 : Lcap;
+        }
+    }
+    if (p.grp_size > 1 && part == 0 && kvh == 0 && threadIdx.x < 32) {
+        // shared-prefix pass: every member's table must start with the leader's blocks
+        const int32_t *lead = p.block_tables + (size_t)s * p.table_stride;
+        bool same = true;
+        for (int m = 1; m < p.grp_size; ++m) {
+            const int32_t *row = lead + (size_t)m * p.max_blocks_per_seq;
+            for (int j = threadIdx.x; j < L / BS; j += 32) same = same && row[j] == lead[j];
+        }
+        if (!same) flag_error(p.d_err, PA_DEVERR_PREFIX);
     }
     const int PT = p.partition_tokens;
     const int nparts = L > 0 ? (L + PT - 1) / PT : 1;
@@ -297,7 +312,7 @@ __global__ void __launch_bounds__(NW * 32, decode_min_ctas<G>()) decode_kernel(c
     __syncwarp();
 
     // ---- step 1 (look up): the unit's first 64 block-table entries
-    const int32_t *table = p.block_tables + (size_t)s * p.max_blocks_per_seq + blk0;
+    const int32_t *table = p.block_tables + (size_t)s * p.table_stride + p.len_offset / BS + blk0;
     const int e0 = lane < nblk ? table[lane] : 0;
     const int e1 = 32 + lane < nblk ? table[32 + lane] : 0;
 
@@ -358,19 +373,25 @@ __global__ void __launch_bounds__(NW * 32, decode_min_ctas<G>()) decode_kernel(c
 
     // ---- query rows of the group in the QK layout, pre-scaled into log2 units
     const int qc = lane % C::QL;
+    // real query/out row of head h of this unit (see DecodeParams)
+    auto row_of = [&](int h) -> size_t {
+        return (size_t)(s * p.grp_size + h / p.grp_inner) * p.num_heads + (size_t)kvh * p.grp_inner +
+               h % p.grp_inner;
+    };
     float2 q2[G][C::CPL][4];
     {
-        const T *qrow = static_cast<const T *>(p.query) + ((size_t)s * p.num_heads + (size_t)kvh * G) * D;
         const float2 sc2 = make_float2(p.scale_log2, p.scale_log2);
 #pragma unroll
-        for (int h = 0; h < G; ++h)
+        for (int h = 0; h < G; ++h) {
+            const T *qrow = static_cast<const T *>(p.query) + row_of(h) * D;
 #pragma unroll
             for (int cc = 0; cc < C::CPL; ++cc) {
-                const uint4 u = *reinterpret_cast<const uint4 *>(qrow + (size_t)h * D + (qc + cc * C::QL) * 8);
+                const uint4 u = *reinterpret_cast<const uint4 *>(qrow + (qc + cc * C::QL) * 8);
                 unpack8x2<T>(u, q2[h][cc]);
 #pragma unroll
                 for (int j = 0; j < 4; ++j) q2[h][cc][j] = __fmul2_rn(q2[h][cc][j], sc2);
             }
+        }
     }
 
     // The one head this lane's owned scores belong to (see ReduceScatter).
@@ -488,15 +509,15 @@ __global__ void __launch_bounds__(NW * 32, decode_min_ctas<G>()) decode_kernel(c
                 o[6] = fmaf(sc, b.z, o[6]); o[7] = fmaf(sc, b.w, o[7]);
             }
         }
-        const int hq = kvh * G + h;
-        if (nparts == 1) {
+        const size_t row = row_of(h);
+        if (nparts == 1 && !p.force_partials) {
             const float inv = lsum > 0.f ? 1.f / lsum : 0.f;
 #pragma unroll
             for (int e = 0; e < 8; ++e) o[e] *= inv;
-            T *orow = static_cast<T *>(p.out) + ((size_t)s * p.num_heads + hq) * D + ch * 8;
+            T *orow = static_cast<T *>(p.out) + row * D + ch * 8;
             *reinterpret_cast<uint4 *>(orow) = pack8<T>(o);
         } else {
-            const size_t slot = ((size_t)s * p.num_heads + hq) * p.max_partitions + part;
+            const size_t slot = row * p.slots + p.part_base + part;
             float4 *dst = reinterpret_cast<float4 *>(p.ws_acc + slot * D + ch * 8);
             dst[0] = make_float4(o[0], o[1], o[2], o[3]);
             dst[1] = make_float4(o[4], o[5], o[6], o[7]);
@@ -514,13 +535,15 @@ __global__ void __launch_bounds__(128) decode_reduce_kernel(const DecodeParams p
     const int pair = blockIdx.x * 4 + warp;
     if (pair >= p.num_seqs * p.num_heads) return;
     const int s = pair / p.num_heads;
-    // same clamping as the decode kernel
-    int L = p.context_lens[s];
-    const int Lcap = min(p.max_context_len, p.max_blocks_per_seq * p.block_size);
+    // same clamping as the decode kernel; slots = the fixed ones plus one per
+    // partition of the sequence's own tokens
+    int L = p.context_lens[s] - p.len_offset;
+    const int Lcap = min(p.max_context_len, p.max_blocks_per_seq * p.block_size) - p.len_offset;
     L = L < 0 ? 0 : (L > Lcap ? Lcap : L);
-    const int nparts = L > 0 ? (L + p.partition_tokens - 1) / p.partition_tokens : 1;
-    if (nparts <= 1) return;
-    const size_t base = (size_t)pair * p.max_partitions;
+    const int own = L > 0 ? (L + p.partition_tokens - 1) / p.partition_tokens : (p.red_fixed_slots > 0 ? 0 : 1);
+    const int nparts = p.red_fixed_slots + own;
+    if (nparts <= 1 && !p.force_partials) return;
+    const size_t base = (size_t)pair * p.slots;
     float M = -INFINITY;
     for (int i = lane; i < nparts; i += 32) M = fmaxf(M, p.ws_ml[base + i].x);
 #pragma unroll
@@ -544,7 +567,7 @@ __global__ void __launch_bounds__(128) decode_reduce_kernel(const DecodeParams p
             o[0] = fmaf(w, x.x, o[0]); o[1] = fmaf(w, x.y, o[1]);
         }
     }
-    const float inv = 1.f / lsum;
+    const float inv = lsum > 0.f ? 1.f / lsum : 0.f;
     T *orow = static_cast<T *>(p.out) + (size_t)pair * D + lane * VPL;
     if constexpr (VPL == 4) {
         uint2 u;
@@ -576,12 +599,22 @@ int launch_decode_t(const DecodeParams &p, cudaStream_t stream) {
     if (units > 0x7fffffffLL) return PA_ERR_UNSUPPORTED;
     kern<<<(unsigned)units, NW * 32, C::SMEM, stream>>>(p);
     if (cudaPeekAtLastError() != cudaSuccess) return PA_ERR_CUDA;
-    if (p.max_partitions > 1) {
+    if (p.max_partitions > 1 && !p.force_partials) {
         const int pairs = p.num_seqs * p.num_heads;
         decode_reduce_kernel<T, D><<<(pairs + 3) / 4, 128, 0, stream>>>(p);
         if (cudaPeekAtLastError() != cudaSuccess) return PA_ERR_CUDA;
     }
     return PA_OK;
+}
+
+template <typename T>
+int launch_reduce_dtype(int head_dim, const DecodeParams &p, cudaStream_t stream) {
+    const int pairs = p.num_seqs * p.num_heads;
+    if (pairs <= 0) return PA_OK;
+    if (head_dim == 128) decode_reduce_kernel<T, 128><<<(pairs + 3) / 4, 128, 0, stream>>>(p);
+    else if (head_dim == 64) decode_reduce_kernel<T, 64><<<(pairs + 3) / 4, 128, 0, stream>>>(p);
+    else return PA_ERR_UNSUPPORTED;
+    return cudaPeekAtLastError() == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }
 
 template <typename T>

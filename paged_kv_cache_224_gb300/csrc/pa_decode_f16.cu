@@ -7,4 +7,7 @@ int launch_decode_f16(int head_dim, int block_size, int group, const DecodeParam
                       cudaStream_t stream) {
     return launch_decode_dtype<__half>(head_dim, block_size, group, p, stream);
 }
+int launch_decode_reduce_f16(int head_dim, const DecodeParams &p, cudaStream_t stream) {
+    return launch_reduce_dtype<__half>(head_dim, p, stream);
+}
 }  // namespace pa

@@ -23,6 +23,18 @@ struct DecodeParams {
     int num_seqs, num_heads, num_kv_heads, max_blocks_per_seq, num_blocks, max_context_len;
     int block_size, partition_tokens, max_partitions;
     float scale_log2;            // scale * log2(e)
+    // Kernel sequence s and its head (kvh, h < G) stand for the real row
+    // ((s*grp_size + h / grp_inner) * num_heads + kvh*grp_inner + h % grp_inner) of
+    // query/out; ordinary decode has grp_size 1 and grp_inner G.  The
+    // shared-prefix pass sets grp_size to the sequences sharing a prefix.
+    int grp_size, grp_inner;
+    int table_stride;            // block-table entries between kernel sequences
+    int len_fixed;               // > 0: every kernel sequence has this many tokens
+    int len_offset;              // tokens before this position are skipped (multiple of block_size)
+    int part_base;               // partials go to partition slot part_base + part ...
+    int slots;                   // ... of `slots` per (row); the reduce merges slots
+    int force_partials;          // write partials even for one-partition units; no reduce
+    int red_fixed_slots;         // reduce: slots before the per-sequence ones
 };
 
 struct PrefillParams {
@@ -43,6 +55,8 @@ int auto_partition_tokens(int num_seqs, int num_kv_heads, int block_size, int ma
 // the shape) or PA_ERR_CUDA (launch / attribute failure).
 int launch_decode(pa_dtype dt, int head_dim, int block_size, int group, const DecodeParams &p,
                   cudaStream_t stream);
+// Log-sum-exp merge of the partials in p's workspace into p.out.
+int launch_decode_reduce(pa_dtype dt, int head_dim, const DecodeParams &p, cudaStream_t stream);
 int launch_reshape_and_cache(const void *key, const void *value, void *k_cache, void *v_cache,
                              const int64_t *slots, int num_tokens, int num_kv_heads, int head_dim,
                              int block_size, int num_blocks, int *d_err, cudaStream_t stream);

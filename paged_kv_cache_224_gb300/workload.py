@@ -60,6 +60,8 @@ class DecodeCase:
     refcounts: np.ndarray             # int32 [NB] how many tables reference each block
     seed: int
     tensors: dict = dataclasses.field(default_factory=dict)
+    group_size: int = 1               # consecutive sequences sharing a prefix (parallel sampling)
+    shared_blocks: int = 0            # full blocks every table of a group starts with
 
     @property
     def max_blocks_per_seq(self) -> int:
@@ -205,7 +207,8 @@ def make_decode_case(name: str, lens: Sequence[int], num_heads: int, num_kv_head
 
 def make_shared_prefix_case(name: str, num_prompts: int, samples: int, prefix_len: int,
                             max_tail: int, num_heads: int, head_dim: int, block_size: int,
-                            dtype: str, seed: int, pool_factor: float = 1.25) -> DecodeCase:
+                            dtype: str, seed: int, pool_factor: float = 1.25,
+                            num_kv_heads: Optional[int] = None) -> DecodeCase:
     """Parallel sampling: each prompt's prefix blocks are referenced by all its samples.
 
     The partial last prefix block (if any) is copy-on-write: samples
@@ -259,8 +262,8 @@ def make_shared_prefix_case(name: str, num_prompts: int, samples: int, prefix_le
     for s in range(B):
         for j in range(blocks_for(lens[s], bs)):
             refc[tables[s, j]] += 1
-    del full
-    return DecodeCase(name=name, num_seqs=B, num_heads=num_heads, num_kv_heads=num_heads,
+    return DecodeCase(name=name, num_seqs=B, num_heads=num_heads,
+                      num_kv_heads=num_heads if num_kv_heads is None else num_kv_heads,
                       head_dim=head_dim, block_size=bs, num_blocks=num_blocks, dtype=dtype,
                       scale=1.0 / math.sqrt(head_dim),
                       context_lens=np.asarray(lens, dtype=np.int32), block_tables=tables,
@@ -268,7 +271,7 @@ def make_shared_prefix_case(name: str, num_prompts: int, samples: int, prefix_le
                       new_token_seq=np.asarray(seqs, dtype=np.int64),
                       new_token_pos=np.asarray(pos, dtype=np.int64),
                       cow_pairs=np.asarray(pairs, dtype=np.int64).reshape(-1, 2),
-                      refcounts=refc, seed=seed)
+                      refcounts=refc, seed=seed, group_size=samples, shared_blocks=full)
 
 
 @dataclasses.dataclass
