@@ -60,7 +60,8 @@ typedef enum {
     PA_ERR_CUDA = -4,          /* a CUDA runtime call failed (launch, attribute) */
     PA_ERR_WORKSPACE = -5,     /* workspace missing or smaller than required */
     PA_ERR_ALIGNMENT = -6,     /* a pointer is not 16-byte aligned */
-    PA_ERR_SCRATCH_LIMIT = -7  /* pa_decode_noalloc: partials exceed its fixed scratch array */
+    PA_ERR_SCRATCH_LIMIT = -7, /* pa_decode_noalloc: partials exceed its fixed scratch array */
+    PA_ERR_NO_BLOCKS = -8      /* block manager: no free block and nothing evictable */
 } pa_status;
 
 /* Size of the device array pa_decode_noalloc keeps its split-K partials in. */
@@ -248,6 +249,60 @@ PA_API int pa_prefill_chunk(void *out, const void *query, const void *k_cache, c
                      const int32_t *block_table, int prefix_len, int chunk_len, int num_heads,
                      int num_kv_heads, int head_dim, int block_size, int num_blocks, float scale,
                      pa_dtype dtype, int *d_err, void *stream);
+
+/*
+ * Block manager -- host bookkeeping of the paged pool: which physical blocks
+ * each sequence's block table holds, reference counts of shared blocks,
+ * copy-on-write, and automatic prefix caching ("vLLM PagedAttention chuyen
+ * sau" (locionic.com), "Tuong tu phan trang bo nho ao" and "Co che APC").
+ * It produces exactly what the kernels consume: block-table rows, slot
+ * mappings for pa_reshape_and_cache and (src, dst) pairs for pa_copy_blocks.
+ * Pure host code; no GPU needed.  Not thread-safe: one owner per manager.
+ *
+ *   pa_bm_create(num_blocks, block_size, enable_prefix_cache)
+ *       -> manager, or NULL on bad sizes.  Free blocks go out in id order.
+ *   pa_bm_add_sequence(m, seq_id, tokens, n, slots, num_cached)
+ *       registers a new sequence with its n prompt token ids.  With prefix
+ *       caching, the longest run of whole blocks whose token ids match blocks
+ *       already cached (a path in the prefix tree) is linked into the table
+ *       and counted as hits; those tokens get slot -1.  Every other token
+ *       gets the slot its K/V must be written to.  Each block that fills up
+ *       joins the prefix tree.  PA_ERR_INVALID_ARG for a known seq_id,
+ *       PA_ERR_NO_BLOCKS (nothing changed) when the pool runs out.
+ *   pa_bm_fork(m, parent, child)
+ *       child starts with all of parent's blocks, shared (parallel sampling).
+ *   pa_bm_append_token(m, seq_id, token, slot, copy_src, copy_dst)
+ *       one more token (decode step): its slot; a new block when the last
+ *       one is full; if the last block is partially filled and shared, a
+ *       private copy first (copy-on-write) whose (src, dst) is returned, else
+ *       src = dst = -1.  The caller copies the block before writing the slot.
+ *   pa_bm_free_sequence(m, seq_id)
+ *       drops the sequence's references.  Unreferenced blocks in the prefix
+ *       tree stay cached (reusable) until evicted; the others are free.
+ *       Allocation evicts the least recently released cached leaf block when
+ *       no free block is left.
+ *   pa_bm_block_table(m, seq_id, out, max_blocks) -> number of blocks, or
+ *       PA_ERR_OUT_OF_RANGE if max_blocks is too small.
+ *   pa_bm_seq_len, pa_bm_block_refcount, pa_bm_stats: introspection.  The
+ *       prefix-cache hit rate is hit_tokens / query_tokens.
+ */
+typedef struct pa_block_manager pa_block_manager;
+typedef struct {
+    int num_blocks, free_blocks, cached_free_blocks, used_blocks, num_sequences;
+    long long query_tokens, hit_tokens, evictions, cow_copies;
+} pa_bm_counters;
+PA_API pa_block_manager *pa_bm_create(int num_blocks, int block_size, int enable_prefix_cache);
+PA_API void pa_bm_destroy(pa_block_manager *m);
+PA_API int pa_bm_add_sequence(pa_block_manager *m, int64_t seq_id, const int32_t *tokens, int num_tokens,
+                              int64_t *slots, int *num_cached_tokens);
+PA_API int pa_bm_fork(pa_block_manager *m, int64_t parent_id, int64_t child_id);
+PA_API int pa_bm_append_token(pa_block_manager *m, int64_t seq_id, int32_t token, int64_t *slot,
+                              int64_t *copy_src, int64_t *copy_dst);
+PA_API int pa_bm_free_sequence(pa_block_manager *m, int64_t seq_id);
+PA_API int pa_bm_block_table(const pa_block_manager *m, int64_t seq_id, int32_t *out, int max_blocks);
+PA_API int64_t pa_bm_seq_len(const pa_block_manager *m, int64_t seq_id);
+PA_API int pa_bm_block_refcount(const pa_block_manager *m, int block);
+PA_API int pa_bm_stats(const pa_block_manager *m, pa_bm_counters *out);
 
 #ifdef __cplusplus
 }

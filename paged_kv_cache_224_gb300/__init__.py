@@ -8,3 +8,4 @@ from .capi import (PAError, lib, pa_copy_blocks, pa_decode, pa_decode_partition_
                    pa_decode_workspace_bytes, pa_prefill_chunk,
                    pa_reshape_and_cache,
                    pa_status_string, decode_workspace)
+from .block_manager import BlockManager  # noqa: F401,E402

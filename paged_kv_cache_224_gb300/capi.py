@@ -23,7 +23,11 @@ DEVERR = {"slot_range": 0x1, "block_range": 0x2, "context_range": 0x4, "copy_pai
           "timeout": 0x10}
 EXPORTED = ("pa_status_string", "pa_reshape_and_cache", "pa_decode_partition_tokens",
             "pa_decode_workspace_bytes", "pa_decode", "pa_copy_blocks", "pa_prefill_chunk",
-            "pa_decode_noalloc", "pa_decode_shared_prefix_workspace_bytes", "pa_decode_shared_prefix")
+            "pa_decode_noalloc", "pa_decode_shared_prefix_workspace_bytes", "pa_decode_shared_prefix",
+            "pa_bm_create", "pa_bm_destroy", "pa_bm_add_sequence", "pa_bm_fork", "pa_bm_append_token",
+            "pa_bm_free_sequence", "pa_bm_block_table", "pa_bm_seq_len", "pa_bm_block_refcount",
+            "pa_bm_stats")
+PA_ERR_NO_BLOCKS = -8
 PA_ERR_SCRATCH_LIMIT = -7
 NOALLOC_SCRATCH_BYTES = 64 << 20
 
@@ -64,6 +68,28 @@ def lib() -> ctypes.CDLL:
         L.pa_decode_shared_prefix.argtypes = [p, p, p, p, p, i, p, i, i, i, i, i, i, i, i, i,
                                               ctypes.c_float, i, i, p, sz, p, p]
         L.pa_decode_shared_prefix.restype = i
+        i64 = ctypes.c_int64
+        L.pa_bm_create.argtypes = [i, i, i]
+        L.pa_bm_create.restype = p
+        L.pa_bm_destroy.argtypes = [p]
+        L.pa_bm_destroy.restype = None
+        L.pa_bm_add_sequence.argtypes = [p, i64, p, i, p, ctypes.POINTER(i)]
+        L.pa_bm_add_sequence.restype = i
+        L.pa_bm_fork.argtypes = [p, i64, i64]
+        L.pa_bm_fork.restype = i
+        L.pa_bm_append_token.argtypes = [p, i64, ctypes.c_int32, ctypes.POINTER(i64), ctypes.POINTER(i64),
+                                         ctypes.POINTER(i64)]
+        L.pa_bm_append_token.restype = i
+        L.pa_bm_free_sequence.argtypes = [p, i64]
+        L.pa_bm_free_sequence.restype = i
+        L.pa_bm_block_table.argtypes = [p, i64, p, i]
+        L.pa_bm_block_table.restype = i
+        L.pa_bm_seq_len.argtypes = [p, i64]
+        L.pa_bm_seq_len.restype = i64
+        L.pa_bm_block_refcount.argtypes = [p, i]
+        L.pa_bm_block_refcount.restype = i
+        L.pa_bm_stats.argtypes = [p, p]
+        L.pa_bm_stats.restype = i
         L.pa_copy_blocks.argtypes = [p, p, p, i, i, i, i, i, i, p, p]
         L.pa_copy_blocks.restype = i
         L.pa_prefill_chunk.argtypes = [p, p, p, p, p, i, i, i, i, i, i, i, ctypes.c_float, i, p, p]

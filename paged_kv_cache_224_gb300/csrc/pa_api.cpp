@@ -81,6 +81,7 @@ const char *pa_status_string(int status) {
     case PA_ERR_ALIGNMENT: return "PA_ERR_ALIGNMENT: pointer not 16-byte aligned";
     case PA_ERR_SCRATCH_LIMIT:
         return "PA_ERR_SCRATCH_LIMIT: split-K partials exceed the fixed scratch of pa_decode_noalloc";
+    case PA_ERR_NO_BLOCKS: return "PA_ERR_NO_BLOCKS: block pool exhausted and nothing evictable";
     default: return "unknown pa_status";
     }
 }
