@@ -221,17 +221,25 @@ def run_prefill_bench(args, world, rank, local, dev, stream):
     then attend the 512-row chunk over its 8192-token paged prefix."""
     import paged_kv_cache_224_gb300 as pa
     from paged_kv_cache_224_gb300 import workload as wl
-    case = wl.chunked_prefill_case(seed=1004 + rank)
+    batch = args.workload == "prefill_batch"
+    case = wl.prefill_batch_case(seed=1005 + rank) if batch else wl.chunked_prefill_case(seed=1004 + rank)
     t = case.materialize(dev)
     slots = torch.as_tensor(case.slot_mapping, device=dev)
-    bt = torch.as_tensor(case.block_table, device=dev)
+    bt = torch.as_tensor(case.block_tables if batch else case.block_table, device=dev)
     out = torch.empty_like(t["query"])
     err = torch.zeros(1, dtype=torch.int32, device=dev)
 
+    def prefill():
+        if batch:
+            pa.pa_prefill_batch(out, t["query"], t["k_cache"], t["v_cache"], bt, case.prefix_lens, case.chunk_lens,
+                                case.scale, d_err=err)
+        else:
+            pa.pa_prefill_chunk(out, t["query"], t["k_cache"], t["v_cache"], bt, case.prefix_len, case.scale,
+                                d_err=err)
+
     def step():
         pa.pa_reshape_and_cache(t["new_key"], t["new_value"], t["k_cache"], t["v_cache"], slots, d_err=err)
-        pa.pa_prefill_chunk(out, t["query"], t["k_cache"], t["v_cache"], bt, case.prefix_len, case.scale,
-                            d_err=err)
+        prefill()
 
     for _ in range(args.warmup):
         step()
@@ -248,8 +256,7 @@ def run_prefill_bench(args, world, rank, local, dev, stream):
         for i in range(args.steps):
             pa.pa_reshape_and_cache(t["new_key"], t["new_value"], t["k_cache"], t["v_cache"], slots, d_err=err)
             ev[i][0].record(stream)
-            pa.pa_prefill_chunk(out, t["query"], t["k_cache"], t["v_cache"], bt, case.prefix_len, case.scale,
-                                d_err=err)
+            prefill()
             ev[i][1].record(stream)
         stop.record(stream)
         torch.cuda.synchronize()
@@ -270,11 +277,14 @@ def run_prefill_bench(args, world, rank, local, dev, stream):
                 "warmup": args.warmup, "ms_per_step": round(elapsed_ms / args.steps, 5),
                 "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": case.dtype,
                 "data": "synthetic",
-                "config": {"workload": case.name, "prefix_len": case.prefix_len, "chunk_len": case.chunk_len,
+                "config": {"workload": case.name,
+                           "prefix_len": case.prefix_lens.tolist() if batch else case.prefix_len,
+                           "chunk_len": case.chunk_lens.tolist() if batch else case.chunk_len,
                            "num_heads": case.num_heads, "num_kv_heads": case.num_kv_heads,
                            "head_dim": case.head_dim, "block_size": case.block_size,
-                           "step": "pa_reshape_and_cache (chunk K/V) + pa_prefill_chunk",
-                           "l2": "KV of one kv head (4.5 MB) is reused from L2 by its row tiles"},
+                           "step": "pa_reshape_and_cache (chunk K/V) + "
+                                   + ("pa_prefill_batch (one launch)" if batch else "pa_prefill_chunk"),
+                           "l2": "each kv head's KV is reused from L2 by its row tiles"},
                 "roofline": {"bound": "tensor", "achieved": round(achieved, 2), "peak": peak,
                              "unit": "TFLOP/s", "frac": round(achieved / peak, 4),
                              "traffic": load_traffic(case.name, "pa_prefill.cu"),
@@ -291,7 +301,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="llama_gqa", choices=["llama_gqa", "opt13b_mha", "long_context", "long_context_bs32",
-                             "shared_prefix", "shared_prefix_grouped", "chunked_prefill"])
+                             "shared_prefix", "shared_prefix_grouped", "chunked_prefill", "prefill_batch"])
     ap.add_argument("--partition-tokens", type=int, default=0)
     ap.add_argument("--e2e-steps", type=int, default=50)
     ap.add_argument("--cpu-seqs", type=int, default=64, help="sequences in the CPU-baseline sample")
@@ -317,7 +327,7 @@ def main():
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
     stream = torch.cuda.current_stream(dev)
-    if args.workload == "chunked_prefill":
+    if args.workload in ("chunked_prefill", "prefill_batch"):
         run_prefill_bench(args, world, rank, local, dev, stream)
         if world > 1:
             import torch.distributed as dist

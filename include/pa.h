@@ -251,6 +251,29 @@ PA_API int pa_prefill_chunk(void *out, const void *query, const void *k_cache, c
                      pa_dtype dtype, int *d_err, void *stream);
 
 /*
+ * pa_prefill_batch -- pa_prefill_chunk for several sequences in one launch
+ * (continuous batching of prompt chunks: "vLLM PagedAttention chuyen sau"
+ * (locionic.com), section "Chunked Prefill").  Sequence i's chunk is rows
+ * row_i .. row_i + chunk_lens[i] - 1 of query and out, where row_i is the sum
+ * of the earlier chunk lengths; its row r (absolute position prefix_lens[i] +
+ * r) attends to keys 0 .. prefix_lens[i] + r of its own block-table row.
+ *
+ *   out, query    [sum(chunk_lens)][num_heads][head_dim] dtype (device)
+ *   block_tables  int32 [num_seqs][max_blocks_per_seq] (device)
+ *   prefix_lens, chunk_lens  int [num_seqs], HOST memory (scheduling
+ *                 metadata the caller knows when it builds the batch); a
+ *                 chunk length of 0 skips the sequence; prefix + chunk must
+ *                 fit in max_blocks_per_seq * block_size
+ * Same numerics, shapes and errors as pa_prefill_chunk; one launch per 64
+ * sequences with a non-empty chunk.
+ */
+PA_API int pa_prefill_batch(void *out, const void *query, const void *k_cache, const void *v_cache,
+                            const int32_t *block_tables, int max_blocks_per_seq, const int *prefix_lens,
+                            const int *chunk_lens, int num_seqs, int num_heads, int num_kv_heads,
+                            int head_dim, int block_size, int num_blocks, float scale, pa_dtype dtype,
+                            int *d_err, void *stream);
+
+/*
  * Block manager -- host bookkeeping of the paged pool: which physical blocks
  * each sequence's block table holds, reference counts of shared blocks,
  * copy-on-write, and automatic prefix caching ("vLLM PagedAttention chuyen

@@ -13,6 +13,8 @@ import ctypes
 import os
 from typing import Optional
 
+import numpy as np
+
 import torch
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -26,7 +28,7 @@ EXPORTED = ("pa_status_string", "pa_reshape_and_cache", "pa_decode_partition_tok
             "pa_decode_noalloc", "pa_decode_shared_prefix_workspace_bytes", "pa_decode_shared_prefix",
             "pa_bm_create", "pa_bm_destroy", "pa_bm_add_sequence", "pa_bm_fork", "pa_bm_append_token",
             "pa_bm_free_sequence", "pa_bm_block_table", "pa_bm_seq_len", "pa_bm_block_refcount",
-            "pa_bm_stats")
+            "pa_bm_stats", "pa_prefill_batch")
 PA_ERR_NO_BLOCKS = -8
 PA_ERR_SCRATCH_LIMIT = -7
 NOALLOC_SCRATCH_BYTES = 64 << 20
@@ -94,6 +96,8 @@ def lib() -> ctypes.CDLL:
         L.pa_copy_blocks.restype = i
         L.pa_prefill_chunk.argtypes = [p, p, p, p, p, i, i, i, i, i, i, i, ctypes.c_float, i, p, p]
         L.pa_prefill_chunk.restype = i
+        L.pa_prefill_batch.argtypes = [p, p, p, p, p, i, p, p, i, i, i, i, i, i, ctypes.c_float, i, p, p]
+        L.pa_prefill_batch.restype = i
         _lib = L
     return _lib
 
@@ -273,3 +277,23 @@ def pa_prefill_chunk(out, query, k_cache, v_cache, block_table, prefix_len, scal
                                 _ptr(block_table), int(prefix_len), C, Hq, Hkv, D, bs, NB,
                                 float(scale), _dt(query), _ptr(d_err), _stream(query, stream))
     _check("pa_prefill_chunk", rc)
+
+
+def pa_prefill_batch(out, query, k_cache, v_cache, block_tables, prefix_lens, chunk_lens, scale,
+                     d_err=None, stream=None):
+    """Several sequences' chunks in one launch.  out/query [sum(chunk_lens)][Hq][D];
+    block_tables int32 [n][MB] on the device; prefix_lens, chunk_lens: n host ints."""
+    _dev(out, query, k_cache, v_cache, block_tables, d_err)
+    if block_tables.dtype != torch.int32:
+        raise TypeError("block_tables must be int32")
+    NB, Hkv, bs, D = k_cache.shape
+    R, Hq, Dq = query.shape
+    pl = np.ascontiguousarray(prefix_lens, dtype=np.int32)
+    cl = np.ascontiguousarray(chunk_lens, dtype=np.int32)
+    n = int(cl.size)
+    if Dq != D or out.shape != query.shape or pl.size != n or block_tables.shape[0] != n or int(cl.sum()) != R:
+        raise ValueError("shape mismatch")
+    rc = lib().pa_prefill_batch(_ptr(out), _ptr(query), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables),
+                                block_tables.shape[1], pl.ctypes.data, cl.ctypes.data, n, Hq, Hkv, D, bs, NB,
+                                float(scale), _dt(query), _ptr(d_err), _stream(query, stream))
+    _check("pa_prefill_batch", rc)

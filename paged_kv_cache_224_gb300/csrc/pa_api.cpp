@@ -314,16 +314,72 @@ int pa_prefill_chunk(void *out, const void *query, const void *k_cache, const vo
     p.query = query;
     p.k_cache = k_cache;
     p.v_cache = v_cache;
-    p.block_table = block_table;
     p.d_err = d_err;
-    p.prefix_len = prefix_len;
-    p.chunk_len = chunk_len;
     p.num_heads = num_heads;
     p.num_kv_heads = num_kv_heads;
     p.num_blocks = num_blocks;
     p.scale_log2 = scale * 1.4426950408889634f;
+    p.num_seqs = 1;
+    p.seqs[0].block_table = block_table;
+    p.seqs[0].prefix_len = prefix_len;
+    p.seqs[0].chunk_len = chunk_len;
+    p.seqs[0].row_start = 0;
     return pa::launch_prefill(dtype, head_dim, block_size, num_heads / num_kv_heads, p,
                               static_cast<cudaStream_t>(stream));
+}
+
+int pa_prefill_batch(void *out, const void *query, const void *k_cache, const void *v_cache,
+                     const int32_t *block_tables, int max_blocks_per_seq, const int *prefix_lens,
+                     const int *chunk_lens, int num_seqs, int num_heads, int num_kv_heads, int head_dim,
+                     int block_size, int num_blocks, float scale, pa_dtype dtype, int *d_err, void *stream) {
+    if (num_seqs < 0 || num_heads <= 0 || num_kv_heads <= 0 || head_dim <= 0 || block_size <= 0 ||
+        num_blocks <= 0 || max_blocks_per_seq <= 0 || !good_dtype(dtype))
+        return PA_ERR_INVALID_ARG;
+    if (num_heads % num_kv_heads) return PA_ERR_INVALID_ARG;
+    if (!std::isfinite(scale) || !(scale > 0.f)) return PA_ERR_OUT_OF_RANGE;
+    if (num_seqs == 0) return PA_OK;
+    if (!prefix_lens || !chunk_lens) return PA_ERR_INVALID_ARG;
+    long long rows = 0;
+    for (int i = 0; i < num_seqs; ++i) {
+        if (prefix_lens[i] < 0 || chunk_lens[i] < 0) return PA_ERR_INVALID_ARG;
+        if ((long long)prefix_lens[i] + chunk_lens[i] > (long long)max_blocks_per_seq * block_size)
+            return PA_ERR_OUT_OF_RANGE;
+        rows += chunk_lens[i];
+    }
+    if (rows == 0) return PA_OK;
+    if (rows > 0x7fffffffLL) return PA_ERR_OUT_OF_RANGE;
+    if (!out || !query || !k_cache || !v_cache || !block_tables) return PA_ERR_INVALID_ARG;
+    if (!aligned16(out) || !aligned16(query) || !aligned16(k_cache) || !aligned16(v_cache))
+        return PA_ERR_ALIGNMENT;
+    pa::PrefillParams p{};
+    p.out = out;
+    p.query = query;
+    p.k_cache = k_cache;
+    p.v_cache = v_cache;
+    p.d_err = d_err;
+    p.num_heads = num_heads;
+    p.num_kv_heads = num_kv_heads;
+    p.num_blocks = num_blocks;
+    p.scale_log2 = scale * 1.4426950408889634f;
+    // sequences with a non-empty chunk, kPrefillMaxSeqs per launch
+    int row = 0;
+    for (int i = 0; i < num_seqs; ++i) {
+        if (chunk_lens[i] > 0) {
+            pa::PrefillSeq &q = p.seqs[p.num_seqs++];
+            q.block_table = block_tables + (size_t)i * max_blocks_per_seq;
+            q.prefix_len = prefix_lens[i];
+            q.chunk_len = chunk_lens[i];
+            q.row_start = row;
+        }
+        row += chunk_lens[i];
+        if (p.num_seqs == pa::kPrefillMaxSeqs || (i == num_seqs - 1 && p.num_seqs > 0)) {
+            const int rc = pa::launch_prefill(dtype, head_dim, block_size, num_heads / num_kv_heads, p,
+                                              static_cast<cudaStream_t>(stream));
+            if (rc != PA_OK) return rc;
+            p.num_seqs = 0;
+        }
+    }
+    return PA_OK;
 }
 
 }  // extern "C"

@@ -37,15 +37,27 @@ struct DecodeParams {
     int red_fixed_slots;         // reduce: slots before the per-sequence ones
 };
 
+// One sequence's chunk in a batched prefill launch.
+struct PrefillSeq {
+    const int32_t *block_table;  // [>= ceil((prefix_len+chunk_len)/bs)]
+    int prefix_len, chunk_len;
+    int row_start;               // first row of the chunk in query/out
+    int cta_start;               // first CTA (grid x) of the sequence; a multiple of the cluster size
+};
+
+constexpr int kPrefillMaxSeqs = 64;  // sequences per launch (kernel-parameter table)
+
 struct PrefillParams {
-    void *out;                   // [C][Hq][D]
-    const void *query;           // [C][Hq][D]
+    void *out;                   // [rows][Hq][D], the chunks one after another
+    const void *query;           // [rows][Hq][D]
     const void *k_cache;
     const void *v_cache;
-    const int32_t *block_table;  // [>= ceil((P+C)/bs)]
     int *d_err;
-    int prefix_len, chunk_len, num_heads, num_kv_heads, num_blocks;
+    int num_heads, num_kv_heads, num_blocks;
     float scale_log2;
+    int num_seqs;                // entries of seqs in use (1 .. kPrefillMaxSeqs)
+    int num_ctas;                // grid x: cta_start of a sequence past the last
+    PrefillSeq seqs[kPrefillMaxSeqs];
 };
 
 // Split-K partition length for the automatic setting.

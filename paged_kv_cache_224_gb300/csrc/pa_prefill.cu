@@ -237,13 +237,20 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int kvh = blockIdx.y;
     const int rank = (int)cluster_rank();
-    const int row0 = blockIdx.x * (kQT * kM);
-    const int nrows = p.chunk_len * G;
+    // the sequence of this CTA: the last one whose first CTA is at or before it
+    int si = 0;
+    for (int i = 1; i < p.num_seqs; ++i)
+        if (p.seqs[i].cta_start <= (int)blockIdx.x) si = i;
+    const PrefillSeq &sq = p.seqs[si];
+    const int prefix_len = sq.prefix_len, chunk_len = sq.chunk_len;
+    const int cta = (int)blockIdx.x - sq.cta_start;  // CTA index within the sequence
+    const int row0 = cta * (kQT * kM);
+    const int nrows = chunk_len * G;
     // both CTAs of a cluster walk the same key tiles: up to the last key any
-    // row of the cluster sees
-    const int cl_row_end = (blockIdx.x - rank + kCluster) * (kQT * kM);
-    const int i_last = min(p.chunk_len - 1, (cl_row_end - 1) / G);
-    const int kend = p.prefix_len + i_last;
+    // row of the cluster sees (cta_start is a multiple of the cluster size)
+    const int cl_row_end = (cta - rank + kCluster) * (kQT * kM);
+    const int i_last = max(0, min(chunk_len - 1, (cl_row_end - 1) / G));
+    const int kend = prefix_len + i_last;
     const int ntiles = kend / kNK + 1;
 
     if (threadIdx.x == 0) {
@@ -276,7 +283,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     if (warp == 0) {
         // ============================================================ producer
-        const int32_t *table = p.block_table;
+        const int32_t *table = sq.block_table;
         const int oob_row = p.num_blocks * p.num_kv_heads * BS;  // first row past the pool: zero fill
         // Table entries come 32 at a time, one per lane, a whole chunk ahead of
         // use (a chunk covers 32 / kBlocksPerTile tiles), so the producer never
@@ -383,16 +390,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int gr = row0 + g * kM + t;
         const bool valid = gr < nrows;
         const int ipos = valid ? gr / G : 0, head = valid ? gr % G : 0;
-        const int plim = p.prefix_len + min(gr / G, p.chunk_len - 1);
-        const int plim_min = p.prefix_len + min((row0 + g * kM) / G, p.chunk_len - 1);  // smallest limit in the tile
+        const int plim = prefix_len + min(gr / G, chunk_len - 1);
+        const int plim_min = prefix_len + min((row0 + g * kM) / G, chunk_len - 1);  // smallest limit in the tile
         const float csc = p.scale_log2;                   // > 0 (checked on the host)
         const uint32_t tS = tmem + kColS + g * kNK + lane_off;
         const uint32_t tO = tmem + kColO + g * kD + lane_off;
 
         // Q row t into the swizzled K-major tile of this group
         {
-            const uint4 *src = reinterpret_cast<const uint4 *>(static_cast<const T *>(p.query) +
-                                                               ((size_t)ipos * p.num_heads + kvh * G + head) * kD);
+            const uint4 *src = reinterpret_cast<const uint4 *>(
+                static_cast<const T *>(p.query) + ((size_t)(sq.row_start + ipos) * p.num_heads + kvh * G + head) * kD);
 #pragma unroll
             for (int c = 0; c < 16; ++c) {
                 const uint4 v = valid ? src[c] : make_uint4(0, 0, 0, 0);
@@ -517,7 +524,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after();
         const float l_run = ((l2[0].x + l2[0].y) + (l2[1].x + l2[1].y)) + ((l2[2].x + l2[2].y) + (l2[3].x + l2[3].y));
         const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
-        T *orow = static_cast<T *>(p.out) + ((size_t)ipos * p.num_heads + kvh * G + head) * kD;
+        T *orow = static_cast<T *>(p.out) + ((size_t)(sq.row_start + ipos) * p.num_heads + kvh * G + head) * kD;
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
             float v[32];
@@ -594,9 +601,8 @@ int launch_tc_t(const PrefillParams &p, cudaStream_t stream) {
     CUtensorMap tmk, tmv;
     if (!make_pool_map(&tmk, p.k_cache, p, BS, bf16) || !make_pool_map(&tmv, p.v_cache, p, BS, bf16))
         return PA_ERR_CUDA;
-    const int tiles = (p.chunk_len * G + kQT * kM - 1) / (kQT * kM);
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((tiles + kCluster - 1) / kCluster * kCluster, p.num_kv_heads);
+    cfg.gridDim = dim3(p.num_ctas, p.num_kv_heads);
     cfg.blockDim = dim3(kThreads);
     cfg.dynamicSmemBytes = kSmemAlloc;
     cfg.stream = stream;
@@ -624,11 +630,25 @@ int launch_tc_dtype(int block_size, int group, const PrefillParams &p, cudaStrea
 
 }  // namespace
 
-int launch_prefill(pa_dtype dt, int head_dim, int block_size, int group, const PrefillParams &p,
+int launch_prefill(pa_dtype dt, int head_dim, int block_size, int group, const PrefillParams &p_in,
                    cudaStream_t stream) {
     if (head_dim != kD) return PA_ERR_UNSUPPORTED;
     // TMA row coordinates are 32-bit
-    if ((long long)p.num_blocks * p.num_kv_heads * block_size >= (1LL << 31)) return PA_ERR_UNSUPPORTED;
+    if ((long long)p_in.num_blocks * p_in.num_kv_heads * block_size >= (1LL << 31)) return PA_ERR_UNSUPPORTED;
+    if (p_in.num_seqs < 1 || p_in.num_seqs > kPrefillMaxSeqs) return PA_ERR_INVALID_ARG;
+    // each sequence's CTAs: its rows (chunk positions x group) in tiles of
+    // kQT*kM, rounded up to whole clusters so no cluster spans two sequences
+    PrefillParams p = p_in;
+    long long ctas = 0;
+    for (int i = 0; i < p.num_seqs; ++i) {
+        p.seqs[i].cta_start = (int)ctas;
+        const long long rows = (long long)p.seqs[i].chunk_len * group;
+        const long long tiles = (rows + kQT * kM - 1) / (kQT * kM);
+        ctas += (tiles + kCluster - 1) / kCluster * kCluster;
+    }
+    if (ctas == 0) return PA_OK;
+    if (ctas > 0x7fffffffLL) return PA_ERR_UNSUPPORTED;
+    p.num_ctas = (int)ctas;
     return dt == PA_BF16 ? launch_tc_dtype<__nv_bfloat16>(block_size, group, p, stream)
                          : launch_tc_dtype<__half>(block_size, group, p, stream);
 }

@@ -347,6 +347,70 @@ def make_prefill_case(name: str, prefix_len: int, chunk_len: int, num_heads: int
                        block_table=table, slot_mapping=slots, seed=seed)
 
 
+@dataclasses.dataclass
+class PrefillBatchCase:
+    """Several sequences' prompt chunks in one step, over one shared pool."""
+    name: str
+    prefix_lens: np.ndarray      # int32 [n]
+    chunk_lens: np.ndarray       # int32 [n]
+    num_heads: int
+    num_kv_heads: int
+    head_dim: int
+    block_size: int
+    num_blocks: int
+    dtype: str
+    scale: float
+    block_tables: np.ndarray     # int32 [n][MB], unused = -1
+    slot_mapping: np.ndarray     # int64 [sum(chunk_lens)] slots of the chunks' tokens, in row order
+    seed: int
+    tensors: dict = dataclasses.field(default_factory=dict)
+
+    def flops(self) -> int:
+        tot = 0
+        for P, C in zip(self.prefix_lens.tolist(), self.chunk_lens.tolist()):
+            tot += C * P + C * (C + 1) // 2
+        return 4 * self.head_dim * tot * self.num_heads
+
+    def materialize(self, device="cpu") -> dict:
+        g = torch.Generator(device=device)
+        g.manual_seed(self.seed)
+        dt = TORCH_DTYPES[self.dtype]
+        shape = (self.num_blocks, self.num_kv_heads, self.block_size, self.head_dim)
+        kc = torch.randn(shape, generator=g, device=device, dtype=dt)
+        vc = torch.randn(shape, generator=g, device=device, dtype=dt)
+        R = int(self.chunk_lens.sum())
+        q = torch.randn((R, self.num_heads, self.head_dim), generator=g, device=device, dtype=dt)
+        nk = torch.randn((R, self.num_kv_heads, self.head_dim), generator=g, device=device, dtype=dt)
+        nv = torch.randn((R, self.num_kv_heads, self.head_dim), generator=g, device=device, dtype=dt)
+        self.tensors = dict(k_cache=kc, v_cache=vc, query=q, new_key=nk, new_value=nv)
+        return self.tensors
+
+
+def make_prefill_batch_case(name: str, prefix_lens, chunk_lens, num_heads: int, num_kv_heads: int,
+                            head_dim: int, block_size: int, dtype: str, seed: int,
+                            pool_factor: float = 1.25) -> PrefillBatchCase:
+    rng = np.random.Generator(np.random.PCG64(seed))
+    P = np.asarray(prefix_lens, dtype=np.int32)
+    C = np.asarray(chunk_lens, dtype=np.int32)
+    need = [blocks_for(int(p + c), block_size) for p, c in zip(P, C)]
+    num_blocks = max(1, int(math.ceil(pool_factor * sum(need))))
+    perm = rng.permutation(num_blocks).astype(np.int32)
+    mb = max(1, max(need))
+    tables = np.full((len(P), mb), -1, dtype=np.int32)
+    at = 0
+    slots = []
+    for i, n in enumerate(need):
+        tables[i, :n] = perm[at:at + n]
+        at += n
+        pos = np.arange(P[i], P[i] + C[i], dtype=np.int64)
+        slots.append(tables[i][pos // block_size].astype(np.int64) * block_size + pos % block_size)
+    return PrefillBatchCase(name=name, prefix_lens=P, chunk_lens=C, num_heads=num_heads,
+                            num_kv_heads=num_kv_heads, head_dim=head_dim, block_size=block_size,
+                            num_blocks=num_blocks, dtype=dtype, scale=1.0 / math.sqrt(head_dim),
+                            block_tables=tables, slot_mapping=np.concatenate(slots) if slots else
+                            np.zeros(0, np.int64), seed=seed)
+
+
 # ---------------------------------------------------------------- workloads
 # The five workloads, named by what they are.  Seeds are 1000 + index.
 
@@ -393,6 +457,15 @@ def chunked_prefill_case(seed: int = 1004) -> PrefillCase:
     return make_prefill_case("prefill_p8192_c512_bf16", prefix_len=8192, chunk_len=512,
                              num_heads=64, num_kv_heads=8, head_dim=128, block_size=16,
                              dtype="bf16", seed=seed)
+
+
+def prefill_batch_case(seed: int = 1005) -> PrefillBatchCase:
+    """Continuous-batching prefill: 8 prompt chunks of mixed sizes after mixed
+    prefixes, LLaMA-style 64/8 heads, bf16, block size 16."""
+    rng = np.random.Generator(np.random.PCG64(seed))
+    chunks = [512, 1024, 256, 2048, 512, 128, 1024, 512]
+    prefixes = [int(x) for x in rng.integers(0, 16384, size=len(chunks))]
+    return make_prefill_batch_case("prefill_batch8_bf16", prefixes, chunks, 64, 8, 128, 16, "bf16", seed=seed)
 
 
 def bits(t: torch.Tensor) -> np.ndarray:

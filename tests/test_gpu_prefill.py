@@ -127,3 +127,92 @@ def test_prefill_ignores_nan_garbage_past_the_chunk(P, C, G, bs):
     out = run_prefill(case, t)
     assert torch.isfinite(out.float()).all()
     check_attention(to_f64(out), ref, "bf16", case.name)
+
+
+BATCHES = [
+    # (prefix_lens, chunk_lens, G, Hkv, bs, dtype)
+    ([40, 0, 333, 1000], [9, 17, 0, 130], 8, 2, 16, "bf16"),   # an empty chunk, a prefix of 0
+    ([100, 64, 7], [64, 1, 200], 2, 2, 32, "f16"),
+    ([0, 0, 0, 0, 0], [3, 300, 17, 64, 1], 4, 1, 16, "bf16"),
+]
+
+
+def _oracle_batch(case, t):
+    kc, vc = wl.bits(t["k_cache"]), wl.bits(t["v_cache"])
+    assert oracle.reshape_and_cache(wl.bits(t["new_key"]), wl.bits(t["new_value"]), kc, vc,
+                                    case.slot_mapping, case.block_size) == 0
+    q = wl.bits(t["query"])
+    refs, row = [], 0
+    for i, (P, C) in enumerate(zip(case.prefix_lens.tolist(), case.chunk_lens.tolist())):
+        if C:
+            refs.append((row, oracle.prefill_chunk(q[row:row + C], kc, vc, case.block_tables[i], P, case.scale,
+                                                   case.dtype, num_threads=8)))
+        row += C
+    return refs
+
+
+def _gpu_batch(case, t):
+    err = torch.zeros(1, dtype=torch.int32, device=DEV)
+    pa.pa_reshape_and_cache(t["new_key"], t["new_value"], t["k_cache"], t["v_cache"],
+                            torch.as_tensor(case.slot_mapping, device=DEV), d_err=err)
+    out = torch.full_like(t["query"], float("nan"))
+    pa.pa_prefill_batch(out, t["query"], t["k_cache"], t["v_cache"], torch.as_tensor(case.block_tables, device=DEV),
+                        case.prefix_lens, case.chunk_lens, case.scale, d_err=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0, f"device error flags {int(err.item()):#x}"
+    return out
+
+
+@pytest.mark.parametrize("P,C,G,Hkv,bs,dtype", BATCHES)
+def test_prefill_batch_matches_oracle_and_single_calls(P, C, G, Hkv, bs, dtype):
+    case = wl.make_prefill_batch_case(f"pfb{len(P)}", P, C, G * Hkv, Hkv, 128, bs, dtype, seed=sum(P) + sum(C))
+    t = case.materialize(DEV)
+    refs = _oracle_batch(case, t)
+    out = _gpu_batch(case, t)
+    for row, ref in refs:
+        check_attention(to_f64(out[row:row + ref.shape[0]]), ref, dtype, f"{case.name} row {row}")
+    # each sequence's rows equal a pa_prefill_chunk call on that sequence alone, bit for bit
+    row = 0
+    for i, (p_, c_) in enumerate(zip(case.prefix_lens.tolist(), case.chunk_lens.tolist())):
+        if c_:
+            one = torch.full_like(out[row:row + c_], float("nan"))
+            pa.pa_prefill_chunk(one, t["query"][row:row + c_].contiguous(), t["k_cache"], t["v_cache"],
+                                torch.as_tensor(case.block_tables[i], device=DEV), p_, case.scale)
+            torch.cuda.synchronize()
+            assert torch.equal(one, out[row:row + c_])
+        row += c_
+
+
+def test_prefill_batch_beyond_one_launch():
+    # 70 sequences: two launches of the per-launch sequence table
+    rng = np.random.default_rng(4)
+    P = [int(x) for x in rng.integers(0, 300, size=70)]
+    C = [int(x) for x in rng.integers(1, 40, size=70)]
+    case = wl.make_prefill_batch_case("pfb70", P, C, 8, 2, 128, 16, "bf16", seed=70)
+    t = case.materialize(DEV)
+    refs = _oracle_batch(case, t)
+    out = _gpu_batch(case, t)
+    for row, ref in refs:
+        check_attention(to_f64(out[row:row + ref.shape[0]]), ref, "bf16", f"row {row}")
+
+
+def test_prefill_batch_full_size_sampled_rows():
+    case = wl.prefill_batch_case()
+    t = case.materialize(DEV)
+    out = _gpu_batch(case, t)
+    assert torch.isfinite(out.float()).all()
+    # sampled rows of two sequences against the oracle (a row is a decode at P+r+1)
+    kc, vc = wl.bits(t["k_cache"]), wl.bits(t["v_cache"])
+    nk, nv = wl.bits(t["new_key"]), wl.bits(t["new_value"])
+    assert oracle.reshape_and_cache(nk, nv, kc, vc, case.slot_mapping, case.block_size) == 0
+    q = wl.bits(t["query"])
+    starts = np.concatenate([[0], np.cumsum(case.chunk_lens)])
+    for i in (0, 3):
+        P, C = int(case.prefix_lens[i]), int(case.chunk_lens[i])
+        for r in (0, C // 2, C - 1):
+            row = int(starts[i]) + r
+            L = P + r + 1
+            n = wl.blocks_for(L, case.block_size)
+            ref = oracle.decode(q[row:row + 1], kc, vc, case.block_tables[i:i + 1, :n],
+                                np.array([L], np.int32), case.scale, case.dtype, num_threads=8)
+            check_attention(to_f64(out[row:row + 1]), ref, case.dtype, f"seq {i} row {r}")
