@@ -93,6 +93,45 @@ def test_cache_calls_reject_bad_arguments_on_host(lib):
     assert lib.pa_prefill_chunk(buf, buf, buf, buf, buf, 8, 4, 7, 2, 128, 16, 64, 0.1, 1, None, None) == -1
 
 
+def test_shared_prefix_and_batch_prefill_reject_bad_arguments_on_host(lib):
+    # all of these return before any CUDA call
+    p = ctypes.c_void_p
+    buf = p(1 << 20)
+    f = ctypes.c_float
+
+    def sp(B=8, S=4, pb=2, Hq=4, Hkv=4, D=128, bs=16, maxlen=100, ws=1 << 30, wsp=buf):
+        return lib.pa_decode_shared_prefix(buf, buf, buf, buf, buf, 16, buf, B, S, pb, Hq, Hkv, D, bs, 64,
+                                           maxlen, f(0.1), 0, 1, wsp, ws, None, None)
+    assert sp(S=3) == -1                       # 8 sequences are not groups of 3
+    assert sp(pb=0) == -1                      # no shared prefix
+    assert sp(pb=20) == -3                     # prefix longer than the table
+    assert sp(Hq=8, Hkv=2, S=4) == -2          # head group 16
+    assert sp(ws=16) == -5                     # workspace too small
+    assert sp(B=0) == 0
+    assert lib.pa_decode_shared_prefix_workspace_bytes(8, 4, 128, 16, 100, 2, 0) > 0
+    assert lib.pa_decode_shared_prefix_workspace_bytes(8, 4, 128, 16, 100, 0, 0) == 0
+
+    pl = (ctypes.c_int * 3)(10, 0, 5)
+    cl = (ctypes.c_int * 3)(4, 0, 3)
+    bad = (ctypes.c_int * 3)(4, -1, 3)
+    big = (ctypes.c_int * 3)(4, 0, 500)
+
+    def pb(prefix=pl, chunk=cl, n=3, Hq=4, Hkv=2, scale=0.1, mb=4):
+        return lib.pa_prefill_batch(buf, buf, buf, buf, buf, mb, prefix, chunk, n, Hq, Hkv, 128, 16, 64,
+                                    f(scale), 1, None, None)
+    assert pb(chunk=bad) == -1                 # negative chunk length
+    assert pb(chunk=big) == -3                 # prefix + chunk past the table row
+    assert pb(Hq=3) == -1
+    assert pb(scale=-1.0) == -3
+    assert pb(n=0) == 0
+    zero = (ctypes.c_int * 3)(0, 0, 0)
+    assert pb(chunk=zero) == 0                 # nothing to attend
+
+
+def test_block_manager_status_strings(lib):
+    assert b"no free block" in lib.pa_status_string(-8) or b"exhausted" in lib.pa_status_string(-8)
+
+
 def test_product_path_has_no_oracle_import():
     # the package must not reach the CPU oracle (only tests, smoke and the
     # benchmark's CPU legs may)
