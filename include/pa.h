@@ -134,7 +134,7 @@ PA_API size_t pa_decode_workspace_bytes(int num_seqs, int num_heads, int head_di
  *                  log-sum-exp reduction (a second kernel on the same stream)
  *   workspace      device buffer of >= pa_decode_workspace_bytes(...) bytes
  *                  (may be NULL when that is 0); its contents are scratch
- * Supported: head_dim in {64, 128}; block_size in {8, 16, 32};
+ * Supported: head_dim in {64, 128}; block_size in {8, 16, 32, 64, 128};
  *   num_heads / num_kv_heads in {1, 2, 4, 8}; dtype f16 or bf16.
  * Invalid lengths are clamped to [0, min(max_context_len,
  * max_blocks_per_seq*block_size)] and flagged; invalid table entries are
@@ -242,7 +242,7 @@ PA_API int pa_copy_blocks(void *k_cache, void *v_cache, const int64_t *pairs, in
  *   query  [chunk_len][num_heads][head_dim] dtype
  *   block_table int32 [>= ceil((prefix_len+chunk_len)/block_size)]
  * scale must be finite and > 0.
- * Supported: head_dim 128, block_size in {16, 32}, group size in {1,2,4,8},
+ * Supported: head_dim 128, block_size in {16, 32, 64, 128}, group size in {1,2,4,8},
  * dtype f16 or bf16.
  */
 PA_API int pa_prefill_chunk(void *out, const void *query, const void *k_cache, const void *v_cache,

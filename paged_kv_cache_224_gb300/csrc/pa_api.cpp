@@ -49,7 +49,7 @@ bool good_dtype(pa_dtype d) { return d == PA_F16 || d == PA_BF16; }
 
 bool decode_shape_supported(int head_dim, int block_size, int group) {
     return (head_dim == 64 || head_dim == 128) &&
-           (block_size == 8 || block_size == 16 || block_size == 32) &&
+           (block_size == 8 || block_size == 16 || block_size == 32 || block_size == 64 || block_size == 128) &&
            (group == 1 || group == 2 || group == 4 || group == 8);
 }
 

@@ -628,9 +628,13 @@ int launch_decode_dtype(int head_dim, int block_size, int group, const DecodePar
     PA_DECODE_GROUPS(128, 16)
     PA_DECODE_GROUPS(128, 32)
     PA_DECODE_GROUPS(128, 8)
+    PA_DECODE_GROUPS(128, 64)
+    PA_DECODE_GROUPS(128, 128)
     PA_DECODE_GROUPS(64, 16)
     PA_DECODE_GROUPS(64, 32)
     PA_DECODE_GROUPS(64, 8)
+    PA_DECODE_GROUPS(64, 64)
+    PA_DECODE_GROUPS(64, 128)
 #undef PA_DECODE_GROUPS
 #undef PA_DECODE_CASE
     return PA_ERR_UNSUPPORTED;

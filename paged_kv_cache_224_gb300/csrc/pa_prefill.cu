@@ -10,9 +10,10 @@
 // the G query heads of one kv head -- against 128-key tiles that both Q tiles
 // share (each K/V byte brought into shared memory serves 256 rows).  CTAs run
 // in clusters of two on adjacent row ranges of the same kv head, and each
-// K/V tile is fetched once for the pair: each CTA copies half of the tile's
-// blocks and multicasts them into both CTAs' shared memory (the TMA unit's
-// cost is per copy, and with 16-row blocks the copies are small).
+// K/V tile is fetched once for the pair: each CTA copies one 64-dim half of
+// every block of the tile and multicasts it into both CTAs' shared memory
+// (the TMA unit's cost is per copy, and with 16-row blocks the copies are
+// small).
 //   warp 0    TMA producer: for each key tile, one 2-D tensor copy per
 //             (block, 64-dim half) of K and of V, straight from the paged pool
 //             into a 128-byte-swizzled shared layout.  K and V have rings of
@@ -215,7 +216,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     constexpr bool kBf16 = std::is_same<T, __nv_bfloat16>::value;
     constexpr int kBlocksPerTile = kNK / BS;
     static_assert(kNK % BS == 0 && kBlocksPerTile <= 32 && 32 % kBlocksPerTile == 0, "block_size");
-    static_assert(kBlocksPerTile % kCluster == 0, "each CTA of a cluster copies the same number of blocks");
+    static_assert(kCluster == 2, "the CTAs of a pair copy one 64-dim half of every block each");
     static_assert(kM % G == 0, "group");
 
     extern __shared__ unsigned char smem_raw[];
@@ -308,10 +309,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                 mbar_arrive_expect_tx(&full[st], (uint32_t)kKVTile);
             }
             __syncwarp();
-            if (lane < kBlocksPerTile && lane % kCluster == rank) {
-                const uint32_t dst = ring + st * kKVTile + lane * BS * 128;
-                tma_2d_mc(dst, map, 0, y, &full[st], kClusterMask);
-                tma_2d_mc(dst + kKVHalf, map, 64, y, &full[st], kClusterMask);
+            if (lane < kBlocksPerTile) {
+                // this CTA's 64-dim half of block `lane`, into both CTAs of the pair
+                const uint32_t dst = ring + st * kKVTile + rank * kKVHalf + lane * BS * 128;
+                tma_2d_mc(dst, map, rank * 64, y, &full[st], kClusterMask);
             }
         };
         // order: K(0), then K(j) before V(j-1) -- both are first needed by the
@@ -623,6 +624,8 @@ int launch_tc_dtype(int block_size, int group, const PrefillParams &p, cudaStrea
 #define PA_TC_GROUPS(BB) PA_TC_CASE(BB, 1) PA_TC_CASE(BB, 2) PA_TC_CASE(BB, 4) PA_TC_CASE(BB, 8)
     PA_TC_GROUPS(16)
     PA_TC_GROUPS(32)
+    PA_TC_GROUPS(64)
+    PA_TC_GROUPS(128)
 #undef PA_TC_GROUPS
 #undef PA_TC_CASE
     return PA_ERR_UNSUPPORTED;

@@ -72,7 +72,8 @@ def test_decode_rejects_bad_arguments_on_host(lib):
     assert call_decode(lib, out=0) == -1                  # null pointer
     assert call_decode(lib, Hq=7) == -1                   # Hq % Hkv != 0
     assert call_decode(lib, D=96) == -2                   # unsupported head_dim
-    assert call_decode(lib, bs=64) == -2                  # unsupported block_size
+    assert call_decode(lib, bs=24) == -2                  # unsupported block_size
+    assert call_decode(lib, bs=256) == -2
     assert call_decode(lib, Hq=32, Hkv=2) == -2           # group 16 unsupported
     assert call_decode(lib, dt=7) == -1                   # bad dtype
     assert call_decode(lib, query=(1 << 20) + 2) == -6    # misaligned

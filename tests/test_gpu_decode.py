@@ -83,6 +83,10 @@ SHAPES = [
     (64, 16, 4, 2, "bf16"),
     (64, 32, 2, 2, "f16"),
     (64, 8, 8, 1, "bf16"),
+    (128, 64, 4, 2, "bf16"),
+    (128, 128, 8, 1, "f16"),
+    (64, 64, 2, 2, "f16"),
+    (64, 128, 1, 2, "bf16"),
 ]
 
 

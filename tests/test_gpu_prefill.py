@@ -47,6 +47,8 @@ CASES = [
     (333, 77, 1, 3, 16, "f16"),
     (1000, 130, 4, 2, 32, "bf16"),
     (64, 1, 8, 1, 16, "bf16"),
+    (200, 150, 2, 2, 64, "bf16"),
+    (300, 70, 8, 1, 128, "f16"),
 ]
 
 
