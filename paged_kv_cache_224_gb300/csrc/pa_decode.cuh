@@ -72,30 +72,30 @@ struct DecodeCfg {
     static_assert(MULTI ? (TR % BS == 0 && BPT <= 4) : (BS % TR == 0), "block_size");
     static_assert(TR % QRP == 0 && NQ % NQS == 0 && STEP_ROWS % TPI == 0, "tile rows");
     static_assert(G <= QL, "group larger than lanes per row");
+    static_assert((G & (G - 1)) == 0 && (NQS & (NQS - 1)) == 0 && (QL & (QL - 1)) == 0,
+                  "the reduce-scatter relabelling XORs indices");
     static_assert((HDR + G * D) * 4 <= RING_BYTES, "merge area must fit in one warp's ring");
     static_assert(NW * 32 >= G * (D / 8), "merge needs one thread per (head, 8 dims)");
     static_assert(OFF_PBUF % 16 == 0, "alignment");
 };
 
 // Shuffle reduce-scatter across the lanes of a row group (xor masks M, M/2,
-// .., 1).  Each halving step keeps one half of the array and adds the
-// partner's copy of it; when one value is left the remaining steps are a
-// plain all-reduce.  Afterwards lane c of the group holds original index
-// f + R*c (f < R) if N >= group size, else index c / (group size / N).
+// .., 1).  Each halving step keeps the low half of the array and adds the
+// partner's high half; when one value is left the remaining steps are a plain
+// all-reduce.  For that to add like to like, every lane lays its partial dots
+// out under its own relabelling: array slot k holds the dot for (head, row)
+// index k XOR base, where base is the index the lane ends up owning -- R*c
+// for lane c of the group if N >= group size, else c / (group size / N) --
+// so partners, which differ in one bit of base, send exactly what the other
+// keeps.  Afterwards lane c holds indices base + f (f < R).
 template <int N, int M>
 struct ReduceScatter {
     static __device__ __forceinline__ void run(float *v, int lane) {
         if constexpr (M == 0) {
             return;
         } else if constexpr (N > 1) {
-            const bool upper = (lane & M) != 0;
 #pragma unroll
-            for (int k = 0; k < N / 2; ++k) {
-                const float a = v[k], b = v[k + N / 2];
-                const float send = upper ? a : b;
-                const float keep = upper ? b : a;
-                v[k] = keep + __shfl_xor_sync(kFull, send, M);
-            }
+            for (int k = 0; k < N / 2; ++k) v[k] += __shfl_xor_sync(kFull, v[k + N / 2], M);
             ReduceScatter<N / 2, M / 2>::run(v, lane);
         } else {
             v[0] += __shfl_xor_sync(kFull, v[0], M);
@@ -142,7 +142,7 @@ __device__ __forceinline__ void attend_tile(const unsigned char *Ks, const unsig
         // QK partial dots over this lane's CPL*8 dims, head-major v[h*NQS + i]
 #pragma unroll
         for (int i = 0; i < C::NQS; ++i) {
-            const int row = step * C::STEP_ROWS + i * C::QRP + qr;
+            const int row = step * C::STEP_ROWS + (i ^ (idx0 % C::NQS)) * C::QRP + qr;  // relabelled row
             float2 a[G];
 #pragma unroll
             for (int cc = 0; cc < C::CPL; ++cc) {
@@ -378,12 +378,18 @@ __global__ void __launch_bounds__(NW * 32, decode_min_ctas<G>()) decode_kernel(c
         return (size_t)(s * p.grp_size + h / p.grp_inner) * p.num_heads + (size_t)kvh * p.grp_inner +
                h % p.grp_inner;
     };
+    // The (head, row) index this lane's scores end with (see ReduceScatter);
+    // its slot h of q2 holds head h XOR (idx0 / NQS), its K row i is row i XOR
+    // (idx0 % NQS).
+    const int idx0 = C::N >= C::QL ? C::R * qc : qc / C::DUP;
+    const int h_lane = idx0 / C::NQS;
+    const bool owner = C::N >= C::QL || (qc % C::DUP) == 0;
     float2 q2[G][C::CPL][4];
     {
         const float2 sc2 = make_float2(p.scale_log2, p.scale_log2);
 #pragma unroll
         for (int h = 0; h < G; ++h) {
-            const T *qrow = static_cast<const T *>(p.query) + row_of(h) * D;
+            const T *qrow = static_cast<const T *>(p.query) + row_of(h ^ h_lane) * D;
 #pragma unroll
             for (int cc = 0; cc < C::CPL; ++cc) {
                 const uint4 u = *reinterpret_cast<const uint4 *>(qrow + (qc + cc * C::QL) * 8);
@@ -394,10 +400,6 @@ __global__ void __launch_bounds__(NW * 32, decode_min_ctas<G>()) decode_kernel(c
         }
     }
 
-    // The one head this lane's owned scores belong to (see ReduceScatter).
-    const int idx0 = C::N >= C::QL ? C::R * qc : qc / C::DUP;
-    const int h_lane = idx0 / C::NQS;
-    const bool owner = C::N >= C::QL || (qc % C::DUP) == 0;
 
     WarpState<G> st;
 #pragma unroll
