@@ -351,14 +351,14 @@ def main():
     # entry point (each group's prefix blocks read once)
     grouped = args.workload == "shared_prefix_grouped"
     if grouped:
-        n = pa.pa_decode_shared_prefix_workspace_bytes(case.num_seqs, case.num_heads, case.head_dim,
+        n = pa.pa_decode_shared_prefix_workspace_bytes(case.num_seqs, case.num_heads, case.num_kv_heads, case.head_dim,
                                                        case.block_size, case.max_context_len,
                                                        case.shared_blocks, pt)
         ws = torch.empty(max(n, 1), dtype=torch.uint8, device=dev)
     else:
-        ws = pa.decode_workspace(t["query"], case.block_size, case.max_context_len, pt)
+        ws = pa.decode_workspace(t["query"], case.num_kv_heads, case.block_size, case.max_context_len, pt)
     err = torch.zeros(1, dtype=torch.int32, device=dev)
-    part = pa.pa_decode_partition_tokens(case.num_seqs, case.num_kv_heads, case.block_size,
+    part = pa.pa_decode_partition_tokens(case.num_seqs, case.num_heads, case.num_kv_heads, case.block_size,
                                          case.max_context_len, pt)
     max_parts = -(-case.max_context_len // part)
     pairs = torch.as_tensor(case.cow_pairs, device=dev) if case.cow_pairs.shape[0] else None

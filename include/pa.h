@@ -99,10 +99,13 @@ PA_API int pa_reshape_and_cache(const void *key, const void *value, void *k_cach
 /*
  * pa_decode_partition_tokens -- the split-K partition length pa_decode uses
  * for these arguments: partition_tokens itself when > 0, otherwise the
- * automatic choice.  Returns 0 when the arguments are invalid.
+ * automatic choice (a power of two in [256, 4096] that grows with
+ * num_seqs * max_context_len * num_kv_heads, so units stay few and long when
+ * the batch alone fills the GPU and get shorter when it does not).  Returns 0
+ * when the arguments are invalid.
  */
-PA_API int pa_decode_partition_tokens(int num_seqs, int num_kv_heads, int block_size,
-                               int max_context_len, int partition_tokens);
+PA_API int pa_decode_partition_tokens(int num_seqs, int num_heads, int num_kv_heads, int block_size,
+                                      int max_context_len, int partition_tokens);
 
 /*
  * pa_decode_workspace_bytes -- device workspace pa_decode needs for split-K
@@ -110,8 +113,8 @@ PA_API int pa_decode_partition_tokens(int num_seqs, int num_kv_heads, int block_
  * Layout (internal): fp32 partial accumulators and (max, sum) pairs per
  * (sequence, query head, partition).
  */
-PA_API size_t pa_decode_workspace_bytes(int num_seqs, int num_heads, int head_dim, int block_size,
-                                 int max_context_len, int partition_tokens);
+PA_API size_t pa_decode_workspace_bytes(int num_seqs, int num_heads, int num_kv_heads, int head_dim,
+                                        int block_size, int max_context_len, int partition_tokens);
 
 /*
  * pa_decode -- single-query paged attention (one decode step).
@@ -172,8 +175,8 @@ PA_API int pa_decode(void *out, const void *query, const void *k_cache, const vo
  * group's queries over its shared blocks as one head group, one pass attends
  * each sequence over its own tokens, and a log-sum-exp merge combines them.
  */
-PA_API size_t pa_decode_shared_prefix_workspace_bytes(int num_seqs, int num_heads, int head_dim,
-                                                      int block_size, int max_context_len,
+PA_API size_t pa_decode_shared_prefix_workspace_bytes(int num_seqs, int num_heads, int num_kv_heads,
+                                                      int head_dim, int block_size, int max_context_len,
                                                       int prefix_blocks, int partition_tokens);
 PA_API int pa_decode_shared_prefix(void *out, const void *query, const void *k_cache,
                                    const void *v_cache, const int32_t *block_tables,

@@ -55,9 +55,9 @@ def lib() -> ctypes.CDLL:
         L.pa_status_string.restype = ctypes.c_char_p
         L.pa_reshape_and_cache.argtypes = [p, p, p, p, p, i, i, i, i, i, i, p, p]
         L.pa_reshape_and_cache.restype = i
-        L.pa_decode_partition_tokens.argtypes = [i, i, i, i, i]
+        L.pa_decode_partition_tokens.argtypes = [i, i, i, i, i, i]
         L.pa_decode_partition_tokens.restype = i
-        L.pa_decode_workspace_bytes.argtypes = [i, i, i, i, i, i]
+        L.pa_decode_workspace_bytes.argtypes = [i, i, i, i, i, i, i]
         L.pa_decode_workspace_bytes.restype = sz
         L.pa_decode.argtypes = [p, p, p, p, p, i, p, i, i, i, i, i, i, i, ctypes.c_float, i, i,
                                 p, sz, p, p]
@@ -65,7 +65,7 @@ def lib() -> ctypes.CDLL:
         L.pa_decode_noalloc.argtypes = [p, p, p, p, p, i, p, i, i, i, i, i, i, i, ctypes.c_float,
                                         i, i, p, p]
         L.pa_decode_noalloc.restype = i
-        L.pa_decode_shared_prefix_workspace_bytes.argtypes = [i, i, i, i, i, i, i]
+        L.pa_decode_shared_prefix_workspace_bytes.argtypes = [i, i, i, i, i, i, i, i]
         L.pa_decode_shared_prefix_workspace_bytes.restype = sz
         L.pa_decode_shared_prefix.argtypes = [p, p, p, p, p, i, p, i, i, i, i, i, i, i, i, i,
                                               ctypes.c_float, i, i, p, sz, p, p]
@@ -154,22 +154,22 @@ def pa_reshape_and_cache(key, value, k_cache, v_cache, slot_mapping, d_err=None,
     _check("pa_reshape_and_cache", rc)
 
 
-def pa_decode_partition_tokens(num_seqs, num_kv_heads, block_size, max_context_len,
+def pa_decode_partition_tokens(num_seqs, num_heads, num_kv_heads, block_size, max_context_len,
                                partition_tokens=0) -> int:
-    return lib().pa_decode_partition_tokens(num_seqs, num_kv_heads, block_size, max_context_len,
+    return lib().pa_decode_partition_tokens(num_seqs, num_heads, num_kv_heads, block_size, max_context_len,
                                             partition_tokens)
 
 
-def pa_decode_workspace_bytes(num_seqs, num_heads, head_dim, block_size, max_context_len,
+def pa_decode_workspace_bytes(num_seqs, num_heads, num_kv_heads, head_dim, block_size, max_context_len,
                               partition_tokens=0) -> int:
-    return lib().pa_decode_workspace_bytes(num_seqs, num_heads, head_dim, block_size,
+    return lib().pa_decode_workspace_bytes(num_seqs, num_heads, num_kv_heads, head_dim, block_size,
                                            max_context_len, partition_tokens)
 
 
-def decode_workspace(query, block_size, max_context_len, partition_tokens=0):
+def decode_workspace(query, num_kv_heads, block_size, max_context_len, partition_tokens=0):
     """Allocate (with torch) a workspace big enough for ``pa_decode``."""
     B, Hq, D = query.shape
-    n = pa_decode_workspace_bytes(B, Hq, D, block_size, max_context_len, partition_tokens)
+    n = pa_decode_workspace_bytes(B, Hq, num_kv_heads, D, block_size, max_context_len, partition_tokens)
     return torch.empty(max(n, 1), dtype=torch.uint8, device=query.device)
 
 
@@ -187,7 +187,7 @@ def pa_decode(out, query, k_cache, v_cache, block_tables, context_lens, scale, m
     if not (out.dtype == query.dtype == k_cache.dtype == v_cache.dtype):
         raise TypeError("dtype mismatch")
     if workspace is None:
-        workspace = decode_workspace(query, bs, max_context_len, partition_tokens)
+        workspace = decode_workspace(query, Hkv, bs, max_context_len, partition_tokens)
     rc = lib().pa_decode(_ptr(out), _ptr(query), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables),
                          block_tables.shape[1], _ptr(context_lens), B, Hq, Hkv, D, bs, NB,
                          int(max_context_len), float(scale), int(partition_tokens), _dt(query),
@@ -196,9 +196,9 @@ def pa_decode(out, query, k_cache, v_cache, block_tables, context_lens, scale, m
     _check("pa_decode", rc)
 
 
-def pa_decode_shared_prefix_workspace_bytes(num_seqs, num_heads, head_dim, block_size,
+def pa_decode_shared_prefix_workspace_bytes(num_seqs, num_heads, num_kv_heads, head_dim, block_size,
                                             max_context_len, prefix_blocks, partition_tokens=0) -> int:
-    return lib().pa_decode_shared_prefix_workspace_bytes(num_seqs, num_heads, head_dim, block_size,
+    return lib().pa_decode_shared_prefix_workspace_bytes(num_seqs, num_heads, num_kv_heads, head_dim, block_size,
                                                          max_context_len, prefix_blocks, partition_tokens)
 
 
@@ -217,7 +217,7 @@ def pa_decode_shared_prefix(out, query, k_cache, v_cache, block_tables, context_
     if not (out.dtype == query.dtype == k_cache.dtype == v_cache.dtype):
         raise TypeError("dtype mismatch")
     if workspace is None:
-        n = pa_decode_shared_prefix_workspace_bytes(B, Hq, D, bs, max_context_len, prefix_blocks,
+        n = pa_decode_shared_prefix_workspace_bytes(B, Hq, Hkv, D, bs, max_context_len, prefix_blocks,
                                                     partition_tokens)
         workspace = torch.empty(max(n, 1), dtype=torch.uint8, device=query.device)
     rc = lib().pa_decode_shared_prefix(

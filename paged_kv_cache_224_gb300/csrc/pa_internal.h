@@ -61,7 +61,7 @@ struct PrefillParams {
 };
 
 // Split-K partition length for the automatic setting.
-int auto_partition_tokens(int num_seqs, int num_kv_heads, int block_size, int max_context_len);
+int auto_partition_tokens(int num_seqs, int num_heads, int num_kv_heads, int block_size, int max_context_len);
 
 // Kernel launchers.  Each returns PA_OK, PA_ERR_UNSUPPORTED (no instance for
 // the shape) or PA_ERR_CUDA (launch / attribute failure).

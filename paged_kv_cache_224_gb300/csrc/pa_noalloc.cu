@@ -43,7 +43,7 @@ extern "C" int pa_decode_noalloc(void *out, const void *query, const void *k_cac
                                  int num_blocks, int max_context_len, float scale,
                                  int partition_tokens, pa_dtype dtype, int *d_err, void *stream) {
     // Reject sizes the array cannot hold before touching the device.
-    const size_t need = pa_decode_workspace_bytes(num_seqs, num_heads, head_dim, block_size,
+    const size_t need = pa_decode_workspace_bytes(num_seqs, num_heads, num_kv_heads, head_dim, block_size,
                                                   max_context_len, partition_tokens);
     if (need > PA_NOALLOC_SCRATCH_BYTES) return PA_ERR_SCRATCH_LIMIT;
     void *scratch = nullptr;

@@ -47,14 +47,22 @@ def test_status_strings(lib):
 def test_workspace_and_partition_rules(lib):
     import paged_kv_cache_224_gb300 as pa
     # every sequence fits one partition -> no workspace
-    assert pa.pa_decode_workspace_bytes(4, 4, 64, 16, 64, 0) == 0
-    assert pa.pa_decode_partition_tokens(256, 8, 16, 4096, 0) == 512
-    n = pa.pa_decode_workspace_bytes(256, 32, 128, 16, 4096, 0)
-    parts = 8
+    assert pa.pa_decode_workspace_bytes(4, 4, 4, 64, 16, 64, 0) == 0
+    # the automatic length on the decode workloads: LLaMA GQA, long context, OPT MHA
+    assert pa.pa_decode_partition_tokens(256, 32, 8, 16, 4096, 0) == 1024
+    assert pa.pa_decode_partition_tokens(8, 64, 8, 16, 131072, 0) == 2048
+    assert pa.pa_decode_partition_tokens(64, 40, 40, 16, 2048, 0) == 512
+    # few, short sequences: the shortest partitions; huge batches: the longest
+    assert pa.pa_decode_partition_tokens(1, 8, 8, 16, 1024, 0) == 256
+    assert pa.pa_decode_partition_tokens(4096, 64, 8, 16, 32768, 0) == 4096
+    assert pa.pa_decode_partition_tokens(1, 8, 8, 128, 16, 0) == 256
+    n = pa.pa_decode_workspace_bytes(256, 32, 8, 128, 16, 4096, 0)
+    parts = 4
     assert n >= 256 * 32 * parts * (128 + 2) * 4
     # explicit partitions must be multiples of block_size
-    assert pa.pa_decode_partition_tokens(4, 4, 16, 100, 24) == 0
-    assert pa.pa_decode_partition_tokens(4, 4, 16, 100, 32) == 32
+    assert pa.pa_decode_partition_tokens(4, 4, 4, 16, 100, 24) == 0
+    assert pa.pa_decode_partition_tokens(4, 4, 4, 16, 100, 32) == 32
+    assert pa.pa_decode_partition_tokens(4, 6, 4, 16, 100, 32) == 0   # heads not a multiple of kv heads
 
 
 def call_decode(lib, **kw):
@@ -109,8 +117,8 @@ def test_shared_prefix_and_batch_prefill_reject_bad_arguments_on_host(lib):
     assert sp(Hq=8, Hkv=2, S=4) == -2          # head group 16
     assert sp(ws=16) == -5                     # workspace too small
     assert sp(B=0) == 0
-    assert lib.pa_decode_shared_prefix_workspace_bytes(8, 4, 128, 16, 100, 2, 0) > 0
-    assert lib.pa_decode_shared_prefix_workspace_bytes(8, 4, 128, 16, 100, 0, 0) == 0
+    assert lib.pa_decode_shared_prefix_workspace_bytes(8, 4, 4, 128, 16, 100, 2, 0) > 0
+    assert lib.pa_decode_shared_prefix_workspace_bytes(8, 4, 4, 128, 16, 100, 0, 0) == 0
 
     pl = (ctypes.c_int * 3)(10, 0, 5)
     cl = (ctypes.c_int * 3)(4, 0, 3)

@@ -79,5 +79,5 @@ def test_shared_prefix_full_size():
 @pytest.mark.parametrize("bs", [16, 32])
 def test_long_context_full_size(bs):
     c = wl.long_context_case(block_size=bs)
-    assert pa.pa_decode_partition_tokens(c.num_seqs, c.num_kv_heads, bs, c.max_context_len) == 512
+    assert pa.pa_decode_partition_tokens(c.num_seqs, c.num_heads, c.num_kv_heads, bs, c.max_context_len) == 2048
     full_step_and_check(c, k_samples=3)

@@ -63,7 +63,7 @@ def test_noalloc_matches_pa_decode_on_two_calls(dtype):
     lens_b = [2500, 5, 1024, 1025, 33, 3999]
     for i, lens in enumerate((lens_a, lens_b)):
         c = wl.make_decode_case(f"noalloc{i}", lens, 8, 2, 128, 16, dtype, seed=500 + i)
-        assert pa.pa_decode_workspace_bytes(c.num_seqs, c.num_heads, c.head_dim, c.block_size,
+        assert pa.pa_decode_workspace_bytes(c.num_seqs, c.num_heads, c.num_kv_heads, c.head_dim, c.block_size,
                                             c.max_context_len, 0) > 0
         t = c.materialize(DEV)
         ref, got = _decode_both(c, t, partition_tokens=0)
@@ -76,7 +76,7 @@ def test_noalloc_refuses_sizes_beyond_its_scratch():
     c = wl.make_decode_case("tiny", [8], 4, 1, 128, 16, "bf16", seed=1)
     t = c.materialize(DEV)
     B, Hq, D, bs, maxlen = 512, 64, 128, 16, 131072  # partials far beyond 64 MiB
-    need = pa.pa_decode_workspace_bytes(B, Hq, D, bs, maxlen, 0)
+    need = pa.pa_decode_workspace_bytes(B, Hq, 8, D, bs, maxlen, 0)
     assert need > pa.capi.NOALLOC_SCRATCH_BYTES
     p = ctypes.c_void_p
     rc = pa.lib().pa_decode_noalloc(p(t["query"].data_ptr()), p(t["query"].data_ptr()),
