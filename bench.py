@@ -151,6 +151,8 @@ def barrier(world: int):
 
 def make_case(name: str, seed_offset: int):
     from paged_kv_cache_224_gb300 import workload as wl
+    if name == "tiny":
+        return wl.tiny_case()
     if name == "llama_gqa":
         return wl.llama_gqa_case(seed=1002 + seed_offset)
     if name == "opt13b_mha":
@@ -300,7 +302,7 @@ def main():
     ap.add_argument("--steps", type=int, default=500)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--workload", default="llama_gqa", choices=["llama_gqa", "opt13b_mha", "long_context", "long_context_bs32",
+    ap.add_argument("--workload", default="llama_gqa", choices=["tiny", "llama_gqa", "opt13b_mha", "long_context", "long_context_bs32",
                              "shared_prefix", "shared_prefix_grouped", "chunked_prefill", "prefill_batch"])
     ap.add_argument("--partition-tokens", type=int, default=0)
     ap.add_argument("--e2e-steps", type=int, default=50)
