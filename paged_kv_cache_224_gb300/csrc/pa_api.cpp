@@ -18,10 +18,17 @@ int launch_decode_f16(int head_dim, int block_size, int group, const DecodeParam
 int launch_decode_reduce_bf16(int head_dim, const DecodeParams &p, cudaStream_t stream);
 int launch_decode_reduce_f16(int head_dim, const DecodeParams &p, cudaStream_t stream);
 
+// Head groups of 8 at head_dim 128 run on the tensor cores; every other shape
+// (and that one, should its tensor maps be refused) on the CUDA cores.
 int launch_decode(pa_dtype dt, int head_dim, int block_size, int group, const DecodeParams &p,
                   cudaStream_t stream) {
-    return dt == PA_BF16 ? launch_decode_bf16(head_dim, block_size, group, p, stream)
-                         : launch_decode_f16(head_dim, block_size, group, p, stream);
+    const int rc = launch_decode_tc(dt, head_dim, block_size, group, p, stream);
+    if (rc == PA_ERR_UNSUPPORTED)
+        return dt == PA_BF16 ? launch_decode_bf16(head_dim, block_size, group, p, stream)
+                             : launch_decode_f16(head_dim, block_size, group, p, stream);
+    if (rc != PA_OK) return rc;
+    if (p.max_partitions > 1 && !p.force_partials) return launch_decode_reduce(dt, head_dim, p, stream);
+    return PA_OK;
 }
 
 int launch_decode_reduce(pa_dtype dt, int head_dim, const DecodeParams &p, cudaStream_t stream) {

@@ -67,6 +67,11 @@ int auto_partition_tokens(int num_seqs, int num_heads, int num_kv_heads, int blo
 // the shape) or PA_ERR_CUDA (launch / attribute failure).
 int launch_decode(pa_dtype dt, int head_dim, int block_size, int group, const DecodeParams &p,
                   cudaStream_t stream);
+// Head groups of 8 at head_dim 128 on the tensor cores (the decode kernel
+// only; the caller launches the reduce).  PA_ERR_UNSUPPORTED for any other
+// shape, or when the driver refuses the kernel's tensor maps.
+int launch_decode_tc(pa_dtype dt, int head_dim, int block_size, int group, const DecodeParams &p,
+                     cudaStream_t stream);
 // Log-sum-exp merge of the partials in p's workspace into p.out.
 int launch_decode_reduce(pa_dtype dt, int head_dim, const DecodeParams &p, cudaStream_t stream);
 int launch_reshape_and_cache(const void *key, const void *value, void *k_cache, void *v_cache,

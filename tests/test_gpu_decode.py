@@ -234,6 +234,77 @@ def test_bad_table_entries_and_lengths_are_flagged_not_faulted():
     assert torch.isfinite(out2.float()).all()
 
 
+# Head groups of 8 at head_dim 128 run on the tensor cores (128-key tiles, one
+# 4-D copy per block): the same edge cases again for that kernel.
+TC_SHAPES = [(8, 2, "bf16"), (16, 2, "f16"), (32, 1, "bf16"), (64, 2, "f16"), (128, 1, "bf16")]
+
+
+@pytest.mark.parametrize("bs,Hkv,dtype", TC_SHAPES)
+def test_group8_tensor_core_shapes(bs, Hkv, dtype):
+    lens = [1, 127, 128, 129, 255, 256, 257, bs + 1, 3 * bs + 5, 1000, 2049]
+    c = wl.make_decode_case(f"tc_bs{bs}", lens, 8 * Hkv, Hkv, 128, bs, dtype, seed=100 + bs)
+    parity(c)
+
+
+@pytest.mark.parametrize("pt", [0, 16, 48, 128, 512, 4096])
+def test_group8_partition_size_invariance(pt):
+    # partitions shorter than, equal to and longer than a 128-key tile
+    lens = [1, 17, 300, 1023, 1024, 1025, 2500, 3000]
+    c = wl.make_decode_case("tc_pt", lens, 16, 2, 128, 16, "bf16", seed=78)
+    parity(c, partition_tokens=pt)
+
+
+def test_group8_single_token_context_is_bit_exact():
+    c = wl.make_decode_case("tc_one", [1] * 5, 16, 2, 128, 16, "f16", seed=9)
+    t = c.materialize(DEV)
+    out, _ = gpu_step(c, t)
+    nv = t["new_value"]
+    for s in range(c.num_seqs):
+        for h in range(16):
+            assert torch.equal(out[s, h], nv[s, h // 8])
+
+
+def test_group8_zero_length_and_nan_garbage_outside_context():
+    lens = [0, 5, 128, 129, 0, 700, 16]
+    c = wl.make_decode_case("tc_nan", lens, 8, 1, 128, 16, "bf16", seed=10)
+    stats, out, _ = parity(c, pool_fill=float("nan"))
+    assert (out[0] == 0).all() and (out[4] == 0).all()
+
+
+def test_group8_physical_permutation_gives_identical_bits():
+    c = wl.make_decode_case("tc_perm", [40, 500, 1300, 7], 16, 2, 128, 16, "bf16", seed=11, num_blocks=140)
+    t = c.materialize(DEV)
+    out_a, _ = gpu_step(c, {k: v.clone() for k, v in t.items()})
+    pi = torch.as_tensor(np.random.default_rng(3).permutation(c.num_blocks), device=DEV)
+    t2 = {k: v.clone() for k, v in t.items()}
+    t2["k_cache"] = torch.empty_like(t["k_cache"])
+    t2["v_cache"] = torch.empty_like(t["v_cache"])
+    t2["k_cache"][pi] = t["k_cache"]
+    t2["v_cache"][pi] = t["v_cache"]
+    pin = pi.cpu().numpy()
+    c2 = wl.make_decode_case("tc_perm2", c.context_lens, 16, 2, 128, 16, "bf16", seed=11, num_blocks=140,
+                             tables=np.where(c.block_tables >= 0, pin[np.maximum(c.block_tables, 0)], -1))
+    out_b, _ = gpu_step(c2, t2)
+    assert torch.equal(out_a, out_b)
+
+
+def test_group8_bad_table_entries_are_flagged_not_faulted():
+    c = wl.make_decode_case("tc_bad", [300, 300, 300], 8, 1, 128, 16, "bf16", seed=12)
+    t = c.materialize(DEV)
+    bt = c.block_tables.copy()
+    bt[1, 3] = c.num_blocks + 1000
+    bt[2, 0] = -7
+    out = torch.empty_like(t["query"])
+    err = torch.zeros(1, dtype=torch.int32, device=DEV)
+    pa.pa_decode(out, t["query"], t["k_cache"], t["v_cache"], torch.as_tensor(bt, device=DEV),
+                 torch.as_tensor(c.context_lens, device=DEV), c.scale, c.max_context_len, d_err=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == pa.capi.DEVERR["block_range"]
+    assert torch.isfinite(out[0].float()).all()
+    out2, _ = gpu_step(c, c.materialize(DEV))
+    assert torch.isfinite(out2.float()).all()
+
+
 def test_host_argument_errors_launch_nothing():
     c = wl.make_decode_case("args", [10], 4, 2, 128, 16, "bf16", seed=1)
     t = c.materialize(DEV)

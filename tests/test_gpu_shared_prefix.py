@@ -58,6 +58,8 @@ CASES = [
     (2, 4, 200, 600, 8, 4, 128, 32, "bf16"),   # GQA G=2 x 4 samples, tails over a partition
     (4, 2, 530, 30, 8, 2, 64, 16, "f16"),      # GQA G=4 x 2, prefix spans two partitions, D=64
     (2, 2, 64, 0, 2, 2, 128, 16, "bf16"),      # every tail empty: L == prefix
+    (2, 1, 160, 300, 16, 2, 128, 16, "bf16"),  # GQA G=8, one sample: both passes are group-of-8 decodes
+    (2, 2, 256, 100, 8, 2, 128, 64, "f16"),    # GQA G=4 x 2 samples at block_size 64
 ]
 
 
