@@ -62,6 +62,13 @@ def load_traffic(kernel_key: str, source: str = "pa_decode.cuh"):
     return None
 
 
+def decode_kernel_of(group: int, head_dim: int):
+    """The decode kernel the library runs for a head group, and its source file."""
+    if group in (4, 8) and head_dim == 128:
+        return "decode_tc_kernel", "pa_decode_tc.cu"
+    return "decode_kernel", "pa_decode.cuh"
+
+
 class ClockSampler:
     """Samples SM clocks and throttle reasons with nvidia-smi while running."""
 
@@ -423,7 +430,9 @@ def main():
     dec_avg_ms = statistics.mean(decode_ms)
     dec_achieved = case.decode_bytes() / (dec_avg_ms / 1e3) / 1e9
     kernel_key = f"decode_{case.name}"
-    traffic = load_traffic(kernel_key)
+    G = case.num_heads // case.num_kv_heads
+    kname, ksrc = decode_kernel_of(G, case.head_dim)
+    traffic = load_traffic(kernel_key, ksrc)
 
     # ---- end to end through the C ABI: host buffers in, result out
     h_q = t["query"].cpu().pin_memory()
@@ -488,8 +497,9 @@ def main():
             "context_tokens_per_s": round(float(case.context_lens.sum()) * world / (ms_per_step / 1e3), 1),
             "roofline": {"bound": "hbm", "achieved": round(dec_achieved, 2), "peak": peak,
                          "unit": "GB/s", "frac": round(dec_achieved / peak, 4), "traffic": traffic,
-                         "kernel": "pa_decode_shared_prefix (decode_kernel x2 + decode_reduce_kernel)"
-                                   if grouped else "pa_decode (decode_kernel + decode_reduce_kernel)",
+                         "kernel": "pa_decode_shared_prefix (%s prefix pass + %s tail pass + decode_reduce_kernel)" % (
+                                   decode_kernel_of(G * case.group_size, case.head_dim)[0], kname)
+                                   if grouped else "pa_decode (%s + decode_reduce_kernel)" % kname,
                          "bytes_per_launch": case.decode_bytes(), "avg_ms": round(dec_avg_ms, 5),
                          "peak_kind": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured" else "fallback"},
             "e2e": {"value": round(e2e_gbs, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d,

@@ -1,14 +1,15 @@
-// Paged decode attention for head groups of 8 on the tensor cores (tcgen05).
+// Paged decode attention for head groups of 4 and 8 on the tensor cores
+// (tcgen05).
 //
 // Same operation and work units as the CUDA-core decode kernel (the three
 // steps of the page "vLLM PagedAttention chuyen sau" (locionic.com), section
 // "Co che PagedAttention": look up each logical block in the block table,
-// gather its K/V rows, attend), for the shape where CUDA cores run out of
-// issue slots: with 8 query heads per kv head every K/V byte feeds 8 dot
+// gather its K/V rows, attend), for the shapes where CUDA cores run short of
+// issue slots: with G query heads per kv head every K/V byte feeds G dot
 // products, and the group's scores and weighted sums are small dense
 // contractions.  Keys are the MMA's M dimension, so nothing is padded along
 // the long axis:
-//   S^T[128 keys][16] = K[128 keys][128 dims] . Q^T    (Q: the 8 heads, zero-padded to N = 16)
+//   S^T[128 keys][16] = K[128 keys][128 dims] . Q^T    (Q: the G heads, zero rows up to N = 16)
 //   O^T[128 dims][16] += V^T[128 dims][128 keys] . P^T (V read in place, MN-major)
 // fp32 accumulators in tensor memory; P is rounded to the input type.
 //
@@ -23,11 +24,11 @@
 //   warp 1    MMA issuer (one thread): QK^T of tile j into one of two S
 //             buffers, then O += P V of tile j-1;
 //   warps 2-5 softmax, one thread per key of the tile (= TMEM lane): read the
-//             key's 8 scores, mask keys past the unit, find each head's tile
+//             key's scores for 8 head slots (the G heads, then zero rows), mask keys past the unit, find each head's tile
 //             maximum (warp reduce-scatter, then an exchange across the four
 //             warps), rescale O in TMEM only when a head's maximum grows by
 //             more than 2^8, write P^T for the PV MMA.  At the end each thread
-//             owns one dimension (= TMEM lane of O^T) and writes it for the 8
+//             owns one dimension (= TMEM lane of O^T) and writes it for the G
 //             heads: the normalised output when the unit is a whole sequence,
 //             else the unnormalised partial (acc, running max, sum) that the
 //             log-sum-exp reduce merges.
@@ -43,8 +44,8 @@
 namespace pa {
 namespace {
 
-constexpr int kTG = 8;                    // query heads per kv head
-constexpr int kTN = 16;                   // MMA N: the group padded to the smallest N allowed with M = 128
+constexpr int kTG = 8;                    // head slots: the group's G query heads, then zero rows
+constexpr int kTN = 16;                   // MMA N: the slots padded to the smallest N allowed with M = 128
 constexpr int kTD = 128;                  // head_dim
 constexpr int kTK = 128;                  // keys per tile (M of the QK^T MMA)
 constexpr int kSlot = kTK * kTD * 2;      // 32 KB: one K or V tile
@@ -94,13 +95,14 @@ __device__ __forceinline__ void sts16(uint32_t addr, uint16_t v) {
     asm volatile("st.shared.u16 [%0], %1;" ::"r"(addr), "h"(v) : "memory");
 }
 
-template <typename T, int BS>
+template <typename T, int BS, int G>
 __global__ void __launch_bounds__(kThreads, 2)
     decode_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tmk,
                      const __grid_constant__ CUtensorMap tmv) {
     constexpr bool kBf16 = std::is_same<T, __nv_bfloat16>::value;
     constexpr int kBPT = kTK / BS;  // blocks per tile
     static_assert(kTK % BS == 0 && BS % 8 == 0 && 32 % kBPT == 0, "block_size");
+    static_assert(G >= 1 && G <= kTG, "group");
 
     // ---- unit = (partition, sequence, kv head); partition-major order
     const int per_part = p.num_seqs * p.num_kv_heads;
@@ -145,7 +147,7 @@ __global__ void __launch_bounds__(kThreads, 2)
 
     if (ntiles == 0) {
         // no keys: zeros, or an empty partial (max -inf, sum 0)
-        if (threadIdx.x < kTG * 16) {
+        if (threadIdx.x < G * 16) {
             const int h = threadIdx.x >> 4, c = threadIdx.x & 15;
             const size_t row = row_of(h);
             if (direct) {
@@ -309,10 +311,12 @@ __global__ void __launch_bounds__(kThreads, 2)
         const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
         const float csc = p.scale_log2;
         {
-            // Q^T rows 0-7 = the group's query heads, rows 8-15 zero; P^T rows 8-15 zero
+            // Q^T rows 0..G-1 = the group's query heads, the rest zero; P^T rows 8-15 zero
             const uint4 z = make_uint4(0, 0, 0, 0);
             const int h = t >> 4, c = t & 15;
-            const uint4 q = *reinterpret_cast<const uint4 *>(static_cast<const T *>(p.query) + row_of(h) * kTD + c * 8);
+            const uint4 q = h < G ? *reinterpret_cast<const uint4 *>(static_cast<const T *>(p.query) +
+                                                                     row_of(h) * kTD + c * 8)
+                                  : z;
             sts128(sb + kOffQ + (c >> 3) * 2048 + h * 128 + (((c & 7) ^ h) << 4), q);
             sts128(sb + kOffQ + (c >> 3) * 2048 + (8 + h) * 128 + (((c & 7) ^ h) << 4), z);
 #pragma unroll
@@ -435,16 +439,14 @@ __global__ void __launch_bounds__(kThreads, 2)
         const int d = t;  // O^T row = dimension
         if (direct) {
 #pragma unroll
-            for (int h = 0; h < kTG; h += 2) {
-                const float i0 = lsum[h] > 0.f ? 1.f / lsum[h] : 0.f;
-                const float i1 = lsum[h + 1] > 0.f ? 1.f / lsum[h + 1] : 0.f;
-                const uint32_t w2 = Elem<T>::pack2(o[h] * i0, o[h + 1] * i1);
+            for (int h = 0; h < G; ++h) {
+                const float inv = lsum[h] > 0.f ? 1.f / lsum[h] : 0.f;
+                const uint32_t w2 = Elem<T>::pack2(o[h] * inv, 0.f);
                 *reinterpret_cast<uint16_t *>(static_cast<T *>(p.out) + row_of(h) * kTD + d) = (uint16_t)(w2 & 0xffffu);
-                *reinterpret_cast<uint16_t *>(static_cast<T *>(p.out) + row_of(h + 1) * kTD + d) = (uint16_t)(w2 >> 16);
             }
         } else {
 #pragma unroll
-            for (int h = 0; h < kTG; ++h) {
+            for (int h = 0; h < G; ++h) {
                 const size_t slot = row_of(h) * p.slots + p.part_base + part;
                 p.ws_acc[slot * kTD + d] = o[h];
                 if (d == h) p.ws_ml[slot] = make_float2(m_run[h], lsum[h]);
@@ -480,9 +482,9 @@ bool make_pool_map4(CUtensorMap *map, const void *pool, const DecodeParams &p, i
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <typename T, int BS>
+template <typename T, int BS, int G>
 int launch_tc_t(const DecodeParams &p, cudaStream_t stream) {
-    auto kern = decode_tc_kernel<T, BS>;
+    auto kern = decode_tc_kernel<T, BS, G>;
     static bool attr_set = false;
     if (!attr_set) {
         if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemAlloc) != cudaSuccess)
@@ -500,14 +502,23 @@ int launch_tc_t(const DecodeParams &p, cudaStream_t stream) {
     return cudaPeekAtLastError() == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }
 
-template <typename T>
-int launch_tc_dtype(int block_size, const DecodeParams &p, cudaStream_t stream) {
+template <typename T, int G>
+int launch_tc_group(int block_size, const DecodeParams &p, cudaStream_t stream) {
     switch (block_size) {
-        case 8: return launch_tc_t<T, 8>(p, stream);
-        case 16: return launch_tc_t<T, 16>(p, stream);
-        case 32: return launch_tc_t<T, 32>(p, stream);
-        case 64: return launch_tc_t<T, 64>(p, stream);
-        case 128: return launch_tc_t<T, 128>(p, stream);
+        case 8: return launch_tc_t<T, 8, G>(p, stream);
+        case 16: return launch_tc_t<T, 16, G>(p, stream);
+        case 32: return launch_tc_t<T, 32, G>(p, stream);
+        case 64: return launch_tc_t<T, 64, G>(p, stream);
+        case 128: return launch_tc_t<T, 128, G>(p, stream);
+        default: return PA_ERR_UNSUPPORTED;
+    }
+}
+
+template <typename T>
+int launch_tc_dtype(int block_size, int group, const DecodeParams &p, cudaStream_t stream) {
+    switch (group) {
+        case 4: return launch_tc_group<T, 4>(block_size, p, stream);
+        case 8: return launch_tc_group<T, 8>(block_size, p, stream);
         default: return PA_ERR_UNSUPPORTED;
     }
 }
@@ -516,11 +527,11 @@ int launch_tc_dtype(int block_size, const DecodeParams &p, cudaStream_t stream) 
 
 int launch_decode_tc(pa_dtype dt, int head_dim, int block_size, int group, const DecodeParams &p,
                      cudaStream_t stream) {
-    if (head_dim != kTD || group != kTG) return PA_ERR_UNSUPPORTED;
+    if (head_dim != kTD || !decode_tc_group(group)) return PA_ERR_UNSUPPORTED;
     // TMA coordinates are 32-bit
     if ((long long)p.num_blocks * p.num_kv_heads * (block_size / 8) >= (1LL << 31)) return PA_ERR_UNSUPPORTED;
-    return dt == PA_BF16 ? launch_tc_dtype<__nv_bfloat16>(block_size, p, stream)
-                         : launch_tc_dtype<__half>(block_size, p, stream);
+    return dt == PA_BF16 ? launch_tc_dtype<__nv_bfloat16>(block_size, group, p, stream)
+                         : launch_tc_dtype<__half>(block_size, group, p, stream);
 }
 
 }  // namespace pa

@@ -67,9 +67,13 @@ int auto_partition_tokens(int num_seqs, int num_heads, int num_kv_heads, int blo
 // the shape) or PA_ERR_CUDA (launch / attribute failure).
 int launch_decode(pa_dtype dt, int head_dim, int block_size, int group, const DecodeParams &p,
                   cudaStream_t stream);
-// Head groups of 8 at head_dim 128 on the tensor cores (the decode kernel
-// only; the caller launches the reduce).  PA_ERR_UNSUPPORTED for any other
-// shape, or when the driver refuses the kernel's tensor maps.
+// Groups whose decode runs on the tensor cores at head_dim 128.  Groups of 1
+// and 2 stay on the CUDA cores, which reach the HBM bound there with three
+// CTAs per SM (and reuse shared prefix blocks through L2 better).
+inline bool decode_tc_group(int group) { return group == 4 || group == 8; }
+// Decode on the tensor cores (the decode kernel only; the caller launches the
+// reduce).  PA_ERR_UNSUPPORTED for any other shape, or when the driver
+// refuses the kernel's tensor maps.
 int launch_decode_tc(pa_dtype dt, int head_dim, int block_size, int group, const DecodeParams &p,
                      cudaStream_t stream);
 // Log-sum-exp merge of the partials in p's workspace into p.out.
