@@ -305,6 +305,39 @@ def test_group8_bad_table_entries_are_flagged_not_faulted():
     assert torch.isfinite(out2.float()).all()
 
 
+@pytest.mark.parametrize("G,dtype,pt", [(1, "bf16", 0), (4, "bf16", 0), (4, "f16", 4096), (8, "bf16", 0),
+                                         (8, "f16", 4096)])
+def test_scores_growing_along_the_context_rescale_the_accumulator(G, dtype, pt):
+    # K rows carry a ramp along one direction u and each query points along
+    # +u or -u, so the scores of half the heads climb by ~16 (log2 units) per
+    # 128 keys -- every tile raises the running maximum past the rescale
+    # threshold -- and the other half fall (the maximum stays on the first tile)
+    Hkv, bs, D = 2, 16, 128
+    lens = [3000, 1500, 700, 129, 1]
+    c = wl.make_decode_case(f"grow_g{G}", lens, G * Hkv, Hkv, D, bs, dtype, seed=300 + G)
+    t = c.materialize(DEV)
+    g = torch.Generator(device=DEV).manual_seed(5)
+    u = torch.randn(D, generator=g, device=DEV)
+    u = u / u.norm()
+    blks, ramps = [], []
+    for s, L in enumerate(c.context_lens):
+        for bi in range(wl.blocks_for(int(L), bs)):
+            blks.append(int(c.block_tables[s, bi]))
+            ramps.append(16.0 / 128 * (bi * bs + np.arange(bs)) / c.scale / np.log2(np.e) / 8.0)
+    blk = torch.as_tensor(blks, device=DEV)
+    ramp = torch.as_tensor(np.stack(ramps), dtype=torch.float32, device=DEV)
+    kc = t["k_cache"].float()
+    kc[blk] += ramp[:, None, :, None] * u
+    t["k_cache"].copy_(kc.to(t["k_cache"].dtype))
+    sign = torch.tensor([1.0 if h % 2 == 0 else -1.0 for h in range(G * Hkv)], device=DEV)
+    q = 8.0 * sign[None, :, None] * u + 0.1 * t["query"].float()
+    t["query"].copy_(q.to(t["query"].dtype))
+    import oracle
+    ref = oracle_step(oracle, c, oracle_inputs(c, t, range(c.num_seqs)))
+    out, _ = gpu_step(c, t, partition_tokens=pt)
+    check_attention(to_f64(out), ref, dtype, c.name)
+
+
 def test_host_argument_errors_launch_nothing():
     c = wl.make_decode_case("args", [10], 4, 2, 128, 16, "bf16", seed=1)
     t = c.materialize(DEV)

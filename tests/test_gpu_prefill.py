@@ -218,3 +218,37 @@ def test_prefill_batch_full_size_sampled_rows():
             ref = oracle.decode(q[row:row + 1], kc, vc, case.block_tables[i:i + 1, :n],
                                 np.array([L], np.int32), case.scale, case.dtype, num_threads=8)
             check_attention(to_f64(out[row:row + 1]), ref, case.dtype, f"seq {i} row {r}")
+
+
+@pytest.mark.parametrize("G,dtype", [(8, "bf16"), (2, "f16")])
+def test_prefill_scores_growing_along_the_keys_rescale_the_accumulator(G, dtype):
+    # K rows carry a ramp along one direction u (in the pool for the prefix,
+    # in the chunk's new keys for its own positions) and each query points
+    # along +u or -u: half the heads' scores climb by ~16 (log2 units) per
+    # 128 keys, so every key tile raises each such row's running maximum past
+    # the rescale threshold; the other half fall
+    P, C, Hkv, bs, D = 700, 150, 2, 16, 128
+    case = wl.make_prefill_case(f"pfgrow{G}", P, C, G * Hkv, Hkv, D, bs, dtype, seed=40 + G)
+    t = case.materialize(DEV)
+    g = torch.Generator(device=DEV).manual_seed(6)
+    u = torch.randn(D, generator=g, device=DEV)
+    u = u / u.norm()
+    step = 16.0 / 128 / case.scale / np.log2(np.e) / 8.0  # raw q.k growth per key, for a query 8u
+    nbp = wl.blocks_for(P, bs)
+    blk = torch.as_tensor(case.block_table[:nbp].astype(np.int64), device=DEV)
+    ramp = torch.as_tensor(step * np.arange(nbp * bs).reshape(nbp, bs), dtype=torch.float32, device=DEV)
+    kc = t["k_cache"].float()
+    kc[blk] += ramp[:, None, :, None] * u
+    t["k_cache"].copy_(kc.to(t["k_cache"].dtype))
+    nk = t["new_key"].float() + (step * (P + torch.arange(C, device=DEV)))[:, None, None] * u
+    t["new_key"].copy_(nk.to(t["new_key"].dtype))
+    sign = torch.tensor([1.0 if h % 2 == 0 else -1.0 for h in range(G * Hkv)], device=DEV)
+    q = 8.0 * sign[None, :, None] * u + 0.1 * t["query"].float()
+    t["query"].copy_(q.to(t["query"].dtype))
+    kc0, vc0 = wl.bits(t["k_cache"]), wl.bits(t["v_cache"])
+    assert oracle.reshape_and_cache(wl.bits(t["new_key"]), wl.bits(t["new_value"]), kc0, vc0,
+                                    case.slot_mapping, bs) == 0
+    ref = oracle.prefill_chunk(wl.bits(t["query"]), kc0, vc0, case.block_table, P, case.scale, dtype,
+                               num_threads=8)
+    out = run_prefill(case, t)
+    check_attention(to_f64(out), ref, dtype, case.name)
