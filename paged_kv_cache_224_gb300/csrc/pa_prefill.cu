@@ -316,10 +316,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                              fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
             mx *= csc;
 
-            if (mx > m_run + 8.0f) {
-                if (j >= 1 && m_run != -INFINITY) {
+            // Lazy rescale.  The TMEM loads and stores are warp-collective, so
+            // the warp decides together: lanes whose maximum did not grow past
+            // the threshold scale by 1.
+            const bool up = mx > m_run + 8.0f;
+            if (__any_sync(kFull, up)) {
+                const float m_new = up ? mx : m_run;
+                if (j >= 1) {
                     // S(j) complete means O holds every PV before it: rescale in place
-                    const float alpha = fast_exp2(m_run - mx);
+                    const float alpha = !up ? 1.f : (m_run == -INFINITY ? 0.f : fast_exp2(m_run - m_new));
 #pragma unroll
                     for (int c = 0; c < 4; ++c) {
                         float v[32];
@@ -332,7 +337,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                     for (int e = 0; e < 4; ++e) l2[e] = __fmul2_rn(l2[e], make_float2(alpha, alpha));
                 }
-                m_run = mx;
+                m_run = m_new;
             }
             // pass 2: P row t = 2^(s*scale - max), rounded to the input type,
             // packed over S's first 64 columns (half h goes to columns 32h..32h+31,
