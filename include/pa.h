@@ -124,6 +124,9 @@ PA_API size_t pa_decode_workspace_bytes(int num_seqs, int num_heads, int num_kv_
  *   2. gather K and V rows from those blocks,
  *   3. out[s][h] = sum_j softmax_j(scale * q[s][h] . K_j) V_j,
  * accumulated in fp32 and rounded once to dtype (round to nearest even).
+ * Groups of 4 and 8 at head_dim 128 run on the tensor cores: the products
+ * accumulate in fp32, and the softmax weights are rounded to dtype before
+ * they multiply V (groups of 1 and 2, and head_dim 64, keep them in fp32).
  *
  *   out            [num_seqs][num_heads][head_dim] dtype (written)
  *   query          [num_seqs][num_heads][head_dim] dtype
@@ -141,7 +144,9 @@ PA_API size_t pa_decode_workspace_bytes(int num_seqs, int num_heads, int num_kv_
  *   num_heads / num_kv_heads in {1, 2, 4, 8}; dtype f16 or bf16.
  * Invalid lengths are clamped to [0, min(max_context_len,
  * max_blocks_per_seq*block_size)] and flagged; invalid table entries are
- * flagged and their rows skipped.
+ * flagged and the keys they would supply are left out of the softmax (on
+ * the CUDA-core path at block_size 8, the whole 16-key tile holding such a
+ * block).
  */
 PA_API int pa_decode(void *out, const void *query, const void *k_cache, const void *v_cache,
               const int32_t *block_tables, int max_blocks_per_seq, const int32_t *context_lens,

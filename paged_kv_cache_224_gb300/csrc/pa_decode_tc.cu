@@ -336,14 +336,20 @@ __global__ void __launch_bounds__(kThreads, 2)
             m_run[h] = -INFINITY;
             l_part[h] = 0.f;
         }
+        const int32_t *table = p.block_tables + (size_t)s * p.table_stride + p.len_offset / BS + tok0 / BS;
         for (int j = 0; j < ntiles; ++j) {
             const int b = j & 1;
+            // this key's block must be in the pool (the producer flags a bad
+            // entry and fetches zeros; the key is left out here); the load is
+            // issued before the wait so its latency hides behind it
+            const int key = j * kTK + t;
+            const int ent = key < ntok ? table[key / BS] : -1;
             wait_or_flag(&s_full[b], (uint32_t)(j >> 1) & 1u, p.d_err);
             tc_fence_after();
             float sc[kTG];
             tmem_ld8(tmem + lane_off + kColS + b * kTN, sc);
             tmem_wait_ld();
-            const bool valid = j * kTK + t < ntok;
+            const bool valid = key < ntok && ent >= 0 && ent < p.num_blocks;
 #pragma unroll
             for (int h = 0; h < kTG; ++h) sc[h] = valid ? sc[h] * csc : -INFINITY;
             // each head's maximum over the tile's 128 keys
@@ -388,7 +394,7 @@ __global__ void __launch_bounds__(kThreads, 2)
             float pr[kTG];
 #pragma unroll
             for (int h = 0; h < kTG; ++h) {
-                pr[h] = fast_exp2(sc[h] - m_run[h]);  // masked keys: 2^-inf = 0
+                pr[h] = valid ? fast_exp2(sc[h] - m_run[h]) : 0.f;  // no NaN while every key so far is masked
                 l_part[h] += pr[h];
             }
             // P^T buffer b is free once the PV of tile j-2 completed
@@ -403,7 +409,7 @@ __global__ void __launch_bounds__(kThreads, 2)
                     sts16(pb + (h + 1) * 128 + ((ch ^ (h + 1)) << 4), (uint16_t)(w2 >> 16));
                 }
             }
-            if (j == ntiles - 1 && !valid) {
+            if (j == ntiles - 1 && key >= ntok) {
                 // this key's V row holds whatever the pool has past the
                 // context (possibly NaN, and 0 * NaN poisons O): zero it
                 const int it = item_v(j), sl = it % kSlots;

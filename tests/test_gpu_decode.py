@@ -288,11 +288,12 @@ def test_group8_physical_permutation_gives_identical_bits():
     assert torch.equal(out_a, out_b)
 
 
-def test_group8_bad_table_entries_are_flagged_not_faulted():
+def test_group8_bad_table_entries_are_flagged_and_their_keys_left_out():
+    import oracle
     c = wl.make_decode_case("tc_bad", [300, 300, 300], 8, 1, 128, 16, "bf16", seed=12)
     t = c.materialize(DEV)
     bt = c.block_tables.copy()
-    bt[1, 3] = c.num_blocks + 1000
+    bt[1, 3] = c.num_blocks + 1000       # outside the pool
     bt[2, 0] = -7
     out = torch.empty_like(t["query"])
     err = torch.zeros(1, dtype=torch.int32, device=DEV)
@@ -300,7 +301,17 @@ def test_group8_bad_table_entries_are_flagged_not_faulted():
                  torch.as_tensor(c.context_lens, device=DEV), c.scale, c.max_context_len, d_err=err)
     torch.cuda.synchronize()
     assert int(err.item()) == pa.capi.DEVERR["block_range"]
-    assert torch.isfinite(out[0].float()).all()
+    # leaving a block's 16 keys out equals attention over the table without
+    # that block and 16 fewer tokens (300 = 18*16 + 12, 284 = 17*16 + 12, so
+    # the partial last block lines up)
+    nb = wl.blocks_for(300, 16)
+    tables = np.stack([c.block_tables[0, :nb],
+                       np.concatenate([c.block_tables[1, :3], c.block_tables[1, 4:nb], [-1]]),
+                       np.concatenate([c.block_tables[2, 1:nb], [-1]])]).astype(np.int32)
+    lens = np.array([300, 284, 284], np.int32)
+    ref = oracle.decode(wl.bits(t["query"]), wl.bits(t["k_cache"]), wl.bits(t["v_cache"]), tables, lens,
+                        c.scale, c.dtype, num_threads=8)
+    check_attention(to_f64(out), ref, c.dtype, c.name)
     out2, _ = gpu_step(c, c.materialize(DEV))
     assert torch.isfinite(out2.float()).all()
 
