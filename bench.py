@@ -434,26 +434,28 @@ def main():
     kname, ksrc = decode_kernel_of(G, case.head_dim)
     traffic = load_traffic(kernel_key, ksrc)
 
-    # ---- end to end through the C ABI: host buffers in, result out
-    h_q = t["query"].cpu().pin_memory()
-    h_nk = t["new_key"].cpu().pin_memory()
-    h_nv = t["new_value"].cpu().pin_memory()
-    h_slots = slots.cpu().pin_memory()
-    h_bt = bt.cpu().pin_memory()
-    h_lens = lens.cpu().pin_memory()
+    # ---- end to end through the C ABI's host-input step: every step copies
+    # its inputs from pinned host memory (queries, new K/V, slots, copy pairs,
+    # block tables, lengths), runs the step and copies the output back
+    pin = lambda x: x.cpu().pin_memory()  # noqa: E731
+    h_q, h_nk, h_nv = pin(t["query"]), pin(t["new_key"]), pin(t["new_value"])
+    h_slots, h_bt, h_lens = pin(slots), pin(bt), pin(lens)
+    h_pairs = pin(pairs) if pairs is not None else None
     h_out = torch.empty(out.shape, dtype=out.dtype).pin_memory()
-    d_q, d_nk, d_nv = torch.empty_like(t["query"]), torch.empty_like(t["new_key"]), torch.empty_like(t["new_value"])
-    d_slots, d_bt, d_lens = torch.empty_like(slots), torch.empty_like(bt), torch.empty_like(lens)
-    h2d = sum(x.numel() * x.element_size() for x in (h_q, h_nk, h_nv, h_slots, h_bt, h_lens))
+    h2d = sum(x.numel() * x.element_size() for x in (h_q, h_nk, h_nv, h_slots, h_bt, h_lens, h_pairs)
+              if x is not None)
     d2h = h_out.numel() * h_out.element_size()
+    staging = torch.empty(max(1, pa.pa_decode_step_host_staging_bytes(
+        case.num_seqs, case.num_heads, case.num_kv_heads, case.head_dim, case.block_size, h_bt.shape[1],
+        case.max_context_len, h_nk.shape[0], 0 if h_pairs is None else h_pairs.shape[0],
+        case.group_size if grouped else 0, case.shared_blocks if grouped else 0, pt)), dtype=torch.uint8, device=dev)
 
     def e2e_step():
-        for d, h in ((d_q, h_q), (d_nk, h_nk), (d_nv, h_nv), (d_slots, h_slots), (d_bt, h_bt), (d_lens, h_lens)):
-            d.copy_(h, non_blocking=True)
-        cow()
-        pa.pa_reshape_and_cache(d_nk, d_nv, t["k_cache"], t["v_cache"], d_slots, d_err=err)
-        decode(d_q, d_bt, d_lens)
-        h_out.copy_(out, non_blocking=True)
+        pa.pa_decode_step_host(h_out, h_q, h_nk, h_nv, h_slots, h_bt, h_lens, t["k_cache"], t["v_cache"],
+                               case.scale, case.max_context_len, pairs=h_pairs,
+                               group_size=case.group_size if grouped else 0,
+                               prefix_blocks=case.shared_blocks if grouped else 0, partition_tokens=pt,
+                               staging=staging, d_err=err)
 
     for _ in range(3):
         e2e_step()
@@ -502,7 +504,8 @@ def main():
                                    if grouped else "pa_decode (%s + decode_reduce_kernel)" % kname,
                          "bytes_per_launch": case.decode_bytes(), "avg_ms": round(dec_avg_ms, 5),
                          "peak_kind": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured" else "fallback"},
-            "e2e": {"value": round(e2e_gbs, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d,
+            "e2e": {"value": round(e2e_gbs, 2), "unit": "GB/s", "api": "pa_decode_step_host (C ABI, pinned host buffers)",
+                    "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 5)},
             "gpu_launches": launches_per_step * args.steps,
             "clocks": clk.summary(),

@@ -225,6 +225,49 @@ PA_API int pa_decode_noalloc(void *out, const void *query, const void *k_cache, 
                              pa_dtype dtype, int *d_err, void *stream);
 
 /*
+ * pa_decode_step_host -- one whole decode step whose inputs sit in host
+ * memory, as a scheduler holds them (the step the pages' engine runs per
+ * generated token: copy-on-write of shared blocks, the new tokens' K/V into
+ * their slots, then attention; "vLLM PagedAttention chuyen sau"
+ * (locionic.com), sections "Co che PagedAttention" and "Co che APC").
+ * In order on `stream`: each host input is copied into `staging` (one
+ * cudaMemcpyAsync per input), then pa_copy_blocks (when num_pairs > 0),
+ * pa_reshape_and_cache (when num_new_tokens > 0), pa_decode -- or
+ * pa_decode_shared_prefix when group_size > 1 -- into staging, and the
+ * output is copied to out_host.  All of it is asynchronous: the host buffers
+ * must stay valid and unchanged until the stream has finished the step, and
+ * out_host holds the result only after the caller synchronises.  Host
+ * buffers should be page-locked (pinned) for the copies to be asynchronous.
+ *   out_host           [num_seqs][num_heads][head_dim] dtype (written)
+ *   query_host         [num_seqs][num_heads][head_dim] dtype
+ *   new_key_host, new_value_host  [num_new_tokens][num_kv_heads][head_dim] dtype
+ *   slot_mapping_host  int64 [num_new_tokens] (as for pa_reshape_and_cache)
+ *   pairs_host         int64 [num_pairs][2] (as for pa_copy_blocks; NULL if 0)
+ *   block_tables_host  int32 [num_seqs][max_blocks_per_seq]
+ *   context_lens_host  int32 [num_seqs]
+ *   k_cache, v_cache   the device pool, as for pa_decode
+ *   group_size, prefix_blocks  0 and 0 for plain decode; otherwise as for
+ *                      pa_decode_shared_prefix
+ *   staging            device buffer of >= pa_decode_step_host_staging_bytes
+ *                      (same shape arguments) bytes, 256-byte aligned; its
+ *                      contents are scratch (it also holds the decode workspace)
+ * Returns the first failing call's status (argument checks happen before any
+ * copy is queued); PA_ERR_WORKSPACE if staging is missing or too small.
+ */
+PA_API size_t pa_decode_step_host_staging_bytes(int num_seqs, int num_heads, int num_kv_heads, int head_dim,
+                                                int block_size, int max_blocks_per_seq, int max_context_len,
+                                                int num_new_tokens, int num_pairs, int group_size,
+                                                int prefix_blocks, int partition_tokens);
+PA_API int pa_decode_step_host(void *out_host, const void *query_host, const void *new_key_host,
+                               const void *new_value_host, const int64_t *slot_mapping_host, int num_new_tokens,
+                               const int64_t *pairs_host, int num_pairs, const int32_t *block_tables_host,
+                               int max_blocks_per_seq, const int32_t *context_lens_host, int num_seqs,
+                               int group_size, int prefix_blocks, int num_heads, int num_kv_heads, int head_dim,
+                               int block_size, int num_blocks, void *k_cache, void *v_cache,
+                               int max_context_len, float scale, int partition_tokens, pa_dtype dtype,
+                               void *staging, size_t staging_bytes, int *d_err, void *stream);
+
+/*
  * pa_copy_blocks -- copy-on-write: for each pair (src, dst) of `pairs`
  * (int64 [num_pairs][2]), copy the whole K block and V block (all kv heads)
  * of src to dst, bit-exact.  A pair is skipped and PA_DEVERR_COPY_PAIR set

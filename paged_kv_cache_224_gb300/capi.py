@@ -28,7 +28,7 @@ EXPORTED = ("pa_status_string", "pa_reshape_and_cache", "pa_decode_partition_tok
             "pa_decode_noalloc", "pa_decode_shared_prefix_workspace_bytes", "pa_decode_shared_prefix",
             "pa_bm_create", "pa_bm_destroy", "pa_bm_add_sequence", "pa_bm_fork", "pa_bm_append_token",
             "pa_bm_free_sequence", "pa_bm_block_table", "pa_bm_seq_len", "pa_bm_block_refcount",
-            "pa_bm_stats", "pa_prefill_batch")
+            "pa_bm_stats", "pa_prefill_batch", "pa_decode_step_host_staging_bytes", "pa_decode_step_host")
 PA_ERR_NO_BLOCKS = -8
 PA_ERR_SCRATCH_LIMIT = -7
 NOALLOC_SCRATCH_BYTES = 64 << 20
@@ -98,6 +98,11 @@ def lib() -> ctypes.CDLL:
         L.pa_prefill_chunk.restype = i
         L.pa_prefill_batch.argtypes = [p, p, p, p, p, i, p, p, i, i, i, i, i, i, ctypes.c_float, i, p, p]
         L.pa_prefill_batch.restype = i
+        L.pa_decode_step_host_staging_bytes.argtypes = [i] * 12
+        L.pa_decode_step_host_staging_bytes.restype = sz
+        L.pa_decode_step_host.argtypes = [p, p, p, p, p, i, p, i, p, i, p, i, i, i, i, i, i, i, i, p, p, i,
+                                          ctypes.c_float, i, i, p, sz, p, p]
+        L.pa_decode_step_host.restype = i
         _lib = L
     return _lib
 
@@ -247,6 +252,59 @@ def pa_decode_noalloc(out, query, k_cache, v_cache, block_tables, context_lens, 
                                  Hkv, D, bs, NB, int(max_context_len), float(scale),
                                  int(partition_tokens), _dt(query), _ptr(d_err), _stream(query, stream))
     _check("pa_decode_noalloc", rc)
+
+
+def _host(*ts):
+    for t in ts:
+        if t is not None:
+            if t.is_cuda:
+                raise ValueError("tensor must be in host memory")
+            if not t.is_contiguous():
+                raise ValueError("tensor must be contiguous")
+
+
+def pa_decode_step_host_staging_bytes(num_seqs, num_heads, num_kv_heads, head_dim, block_size, max_blocks_per_seq,
+                                      max_context_len, num_new_tokens, num_pairs=0, group_size=0, prefix_blocks=0,
+                                      partition_tokens=0) -> int:
+    return lib().pa_decode_step_host_staging_bytes(num_seqs, num_heads, num_kv_heads, head_dim, block_size,
+                                                   max_blocks_per_seq, max_context_len, num_new_tokens, num_pairs,
+                                                   group_size, prefix_blocks, partition_tokens)
+
+
+def pa_decode_step_host(out, query, new_key, new_value, slot_mapping, block_tables, context_lens, k_cache,
+                        v_cache, scale, max_context_len, pairs=None, group_size=0, prefix_blocks=0,
+                        partition_tokens=0, staging=None, d_err=None, stream=None):
+    """One decode step from host tensors (pinned for asynchronous copies):
+    out/query [B][Hq][D], new_key/new_value [T][Hkv][D], slot_mapping int64 [T],
+    block_tables int32 [B][MB], context_lens int32 [B], pairs int64 [n][2] or
+    None; the pool (k_cache, v_cache) and ``staging`` are on the device.  The
+    result lands in ``out`` once the stream has finished the step."""
+    _host(out, query, new_key, new_value, slot_mapping, block_tables, context_lens, pairs)
+    _dev(k_cache, v_cache, staging, d_err)
+    if block_tables.dtype != torch.int32 or context_lens.dtype != torch.int32:
+        raise TypeError("block_tables and context_lens must be int32")
+    if slot_mapping.dtype != torch.int64 or (pairs is not None and pairs.dtype != torch.int64):
+        raise TypeError("slot_mapping and pairs must be int64")
+    NB, Hkv, bs, D = k_cache.shape
+    B, Hq, Dq = query.shape
+    T = new_key.shape[0]
+    n = pairs.shape[0] if pairs is not None and pairs.numel() else 0
+    if Dq != D or out.shape != query.shape or block_tables.shape[0] != B or context_lens.shape != (B,) or \
+            new_value.shape != new_key.shape or slot_mapping.shape != (T,):
+        raise ValueError("shape mismatch")
+    if not (out.dtype == query.dtype == new_key.dtype == new_value.dtype == k_cache.dtype == v_cache.dtype):
+        raise TypeError("dtype mismatch")
+    MB = block_tables.shape[1]
+    if staging is None:
+        need = pa_decode_step_host_staging_bytes(B, Hq, Hkv, D, bs, MB, max_context_len, T, n, group_size,
+                                                 prefix_blocks, partition_tokens)
+        staging = torch.empty(max(need, 1), dtype=torch.uint8, device=k_cache.device)
+    rc = lib().pa_decode_step_host(
+        _ptr(out), _ptr(query), _ptr(new_key), _ptr(new_value), _ptr(slot_mapping), T, _ptr(pairs), n,
+        _ptr(block_tables), MB, _ptr(context_lens), B, int(group_size), int(prefix_blocks), Hq, Hkv, D, bs, NB,
+        _ptr(k_cache), _ptr(v_cache), int(max_context_len), float(scale), int(partition_tokens), _dt(query),
+        _ptr(staging), staging.numel() * staging.element_size(), _ptr(d_err), _stream(k_cache, stream))
+    _check("pa_decode_step_host", rc)
 
 
 def pa_copy_blocks(k_cache, v_cache, pairs, d_err=None, stream=None):

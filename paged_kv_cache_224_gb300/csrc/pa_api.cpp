@@ -407,3 +407,123 @@ int pa_prefill_batch(void *out, const void *query, const void *k_cache, const vo
 }
 
 }  // extern "C"
+
+// ---- a whole decode step from host-resident inputs ----------------------------
+
+namespace {
+
+size_t round256(size_t n) { return (n + 255) / 256 * 256; }
+
+// Staging regions of pa_decode_step_host, in order: out, query, new keys, new
+// values, slots, copy pairs, block tables, context lengths, decode workspace.
+struct StepLayout {
+    size_t off[9];
+    size_t total;
+};
+
+bool step_layout(int num_seqs, int num_heads, int num_kv_heads, int head_dim, int block_size,
+                 int max_blocks_per_seq, int max_context_len, int num_new_tokens, int num_pairs, int group_size,
+                 int prefix_blocks, int partition_tokens, StepLayout *lay) {
+    if (num_seqs <= 0 || num_heads <= 0 || num_kv_heads <= 0 || num_heads % num_kv_heads || head_dim <= 0 ||
+        block_size <= 0 || max_blocks_per_seq <= 0 || max_context_len < 0 || num_new_tokens < 0 || num_pairs < 0)
+        return false;
+    const size_t qbytes = (size_t)num_seqs * num_heads * head_dim * 2;
+    const size_t kvbytes = (size_t)num_new_tokens * num_kv_heads * head_dim * 2;
+    size_t ws = 0;
+    if (group_size > 1) {
+        if (prefix_blocks <= 0) return false;
+        ws = pa_decode_shared_prefix_workspace_bytes(num_seqs, num_heads, num_kv_heads, head_dim, block_size,
+                                                     max_context_len, prefix_blocks, partition_tokens);
+    } else {
+        ws = pa_decode_workspace_bytes(num_seqs, num_heads, num_kv_heads, head_dim, block_size, max_context_len,
+                                       partition_tokens);
+    }
+    const size_t sizes[9] = {qbytes, qbytes, kvbytes, kvbytes, (size_t)num_new_tokens * 8,
+                             (size_t)num_pairs * 16, (size_t)num_seqs * max_blocks_per_seq * 4,
+                             (size_t)num_seqs * 4, ws};
+    size_t at = 0;
+    for (int i = 0; i < 9; ++i) {
+        lay->off[i] = at;
+        at += round256(sizes[i]);
+    }
+    lay->total = at;
+    return true;
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t pa_decode_step_host_staging_bytes(int num_seqs, int num_heads, int num_kv_heads, int head_dim,
+                                         int block_size, int max_blocks_per_seq, int max_context_len,
+                                         int num_new_tokens, int num_pairs, int group_size, int prefix_blocks,
+                                         int partition_tokens) {
+    StepLayout lay;
+    if (!step_layout(num_seqs, num_heads, num_kv_heads, head_dim, block_size, max_blocks_per_seq,
+                     max_context_len, num_new_tokens, num_pairs, group_size, prefix_blocks, partition_tokens,
+                     &lay))
+        return 0;
+    return lay.total;
+}
+
+int pa_decode_step_host(void *out_host, const void *query_host, const void *new_key_host,
+                        const void *new_value_host, const int64_t *slot_mapping_host, int num_new_tokens,
+                        const int64_t *pairs_host, int num_pairs, const int32_t *block_tables_host,
+                        int max_blocks_per_seq, const int32_t *context_lens_host, int num_seqs, int group_size,
+                        int prefix_blocks, int num_heads, int num_kv_heads, int head_dim, int block_size,
+                        int num_blocks, void *k_cache, void *v_cache, int max_context_len, float scale,
+                        int partition_tokens, pa_dtype dtype, void *staging, size_t staging_bytes, int *d_err,
+                        void *stream) {
+    if (num_seqs <= 0 || num_blocks <= 0 || !good_dtype(dtype)) return PA_ERR_INVALID_ARG;
+    StepLayout lay;
+    if (!step_layout(num_seqs, num_heads, num_kv_heads, head_dim, block_size, max_blocks_per_seq,
+                     max_context_len, num_new_tokens, num_pairs, group_size, prefix_blocks, partition_tokens,
+                     &lay))
+        return PA_ERR_INVALID_ARG;
+    if (!out_host || !query_host || !block_tables_host || !context_lens_host || !k_cache || !v_cache)
+        return PA_ERR_INVALID_ARG;
+    if (num_new_tokens > 0 && (!new_key_host || !new_value_host || !slot_mapping_host)) return PA_ERR_INVALID_ARG;
+    if (num_pairs > 0 && !pairs_host) return PA_ERR_INVALID_ARG;
+    if (!staging || staging_bytes < lay.total) return PA_ERR_WORKSPACE;
+    if ((reinterpret_cast<uintptr_t>(staging) & 255u) != 0) return PA_ERR_ALIGNMENT;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    char *base = static_cast<char *>(staging);
+    void *d_out = base + lay.off[0], *d_q = base + lay.off[1], *d_k = base + lay.off[2], *d_v = base + lay.off[3];
+    int64_t *d_slots = reinterpret_cast<int64_t *>(base + lay.off[4]);
+    int64_t *d_pairs = reinterpret_cast<int64_t *>(base + lay.off[5]);
+    int32_t *d_bt = reinterpret_cast<int32_t *>(base + lay.off[6]);
+    int32_t *d_lens = reinterpret_cast<int32_t *>(base + lay.off[7]);
+    void *d_ws = base + lay.off[8];
+    const size_t ws_bytes = lay.total - lay.off[8];
+    const size_t qbytes = (size_t)num_seqs * num_heads * head_dim * 2;
+    const size_t kvbytes = (size_t)num_new_tokens * num_kv_heads * head_dim * 2;
+    auto h2d = [&](void *dst, const void *src, size_t n) {
+        return n == 0 || cudaMemcpyAsync(dst, src, n, cudaMemcpyHostToDevice, st) == cudaSuccess;
+    };
+    if (!h2d(d_q, query_host, qbytes) || !h2d(d_k, new_key_host, kvbytes) || !h2d(d_v, new_value_host, kvbytes) ||
+        !h2d(d_slots, slot_mapping_host, (size_t)num_new_tokens * 8) ||
+        !h2d(d_pairs, pairs_host, (size_t)num_pairs * 16) ||
+        !h2d(d_bt, block_tables_host, (size_t)num_seqs * max_blocks_per_seq * 4) ||
+        !h2d(d_lens, context_lens_host, (size_t)num_seqs * 4))
+        return PA_ERR_CUDA;
+    int rc = pa_copy_blocks(k_cache, v_cache, d_pairs, num_pairs, num_kv_heads, head_dim, block_size, num_blocks,
+                            dtype, d_err, stream);
+    if (rc != PA_OK) return rc;
+    rc = pa_reshape_and_cache(d_k, d_v, k_cache, v_cache, d_slots, num_new_tokens, num_kv_heads, head_dim,
+                              block_size, num_blocks, dtype, d_err, stream);
+    if (rc != PA_OK) return rc;
+    if (group_size > 1)
+        rc = pa_decode_shared_prefix(d_out, d_q, k_cache, v_cache, d_bt, max_blocks_per_seq, d_lens, num_seqs,
+                                     group_size, prefix_blocks, num_heads, num_kv_heads, head_dim, block_size,
+                                     num_blocks, max_context_len, scale, partition_tokens, dtype, d_ws, ws_bytes,
+                                     d_err, stream);
+    else
+        rc = pa_decode(d_out, d_q, k_cache, v_cache, d_bt, max_blocks_per_seq, d_lens, num_seqs, num_heads,
+                       num_kv_heads, head_dim, block_size, num_blocks, max_context_len, scale, partition_tokens,
+                       dtype, d_ws, ws_bytes, d_err, stream);
+    if (rc != PA_OK) return rc;
+    return cudaMemcpyAsync(out_host, d_out, qbytes, cudaMemcpyDeviceToHost, st) == cudaSuccess ? PA_OK
+                                                                                                  : PA_ERR_CUDA;
+}
+
+}  // extern "C"

@@ -590,12 +590,8 @@ int launch_decode_t(const DecodeParams &p, cudaStream_t stream) {
     constexpr int S = kDecodeStages;
     using C = DecodeCfg<D, BS, G, NW, S>;
     auto kern = decode_kernel<T, D, BS, G, NW, S>;
-    static bool attr_set = false;
-    if (!attr_set) {
-        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM) != cudaSuccess)
-            return PA_ERR_CUDA;
-        attr_set = true;
-    }
+    static std::atomic<uint64_t> attr_done{0};
+    if (ensure_smem_attr(kern, C::SMEM, attr_done) != PA_OK) return PA_ERR_CUDA;
     const long long units = (long long)p.max_partitions * p.num_seqs * p.num_kv_heads;
     if (units <= 0) return PA_OK;
     if (units > 0x7fffffffLL) return PA_ERR_UNSUPPORTED;

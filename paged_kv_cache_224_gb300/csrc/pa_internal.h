@@ -5,9 +5,25 @@
 #include <stddef.h>
 #include <stdint.h>
 
+#include <atomic>
+
 #include "../../include/pa.h"
 
 namespace pa {
+
+// Raise a kernel's dynamic shared-memory limit once per device (the attribute
+// is per device; `done` is the caller's per-kernel record of devices set).
+template <typename Kernel>
+int ensure_smem_attr(Kernel kern, int bytes, std::atomic<uint64_t> &done) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return PA_ERR_CUDA;
+    const uint64_t bit = 1ull << dev;
+    if (done.load(std::memory_order_acquire) & bit) return PA_OK;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) != cudaSuccess)
+        return PA_ERR_CUDA;
+    done.fetch_or(bit, std::memory_order_release);
+    return PA_OK;
+}
 
 // Everything a decode launch needs; passed by value to the kernels.
 struct DecodeParams {

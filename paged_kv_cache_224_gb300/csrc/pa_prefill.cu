@@ -443,12 +443,8 @@ bool make_pool_map(CUtensorMap *map, const void *pool, const PrefillParams &p, i
 template <typename T, int BS, int G>
 int launch_tc_t(const PrefillParams &p, cudaStream_t stream) {
     auto kern = prefill_tc_kernel<T, BS, G>;
-    static bool attr_set = false;
-    if (!attr_set) {
-        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemAlloc) != cudaSuccess)
-            return PA_ERR_CUDA;
-        attr_set = true;
-    }
+    static std::atomic<uint64_t> attr_done{0};
+    if (ensure_smem_attr(kern, kSmemAlloc, attr_done) != PA_OK) return PA_ERR_CUDA;
     const bool bf16 = std::is_same<T, __nv_bfloat16>::value;
     CUtensorMap tmk, tmv;
     if (!make_pool_map(&tmk, p.k_cache, p, BS, bf16) || !make_pool_map(&tmv, p.v_cache, p, BS, bf16))

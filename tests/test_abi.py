@@ -137,6 +137,31 @@ def test_shared_prefix_and_batch_prefill_reject_bad_arguments_on_host(lib):
     assert pb(chunk=zero) == 0                 # nothing to attend
 
 
+def test_host_step_rejects_bad_arguments_on_host(lib):
+    # every check happens before any copy is queued
+    p = ctypes.c_void_p
+    buf = p(1 << 20)
+    f = ctypes.c_float
+    need = lib.pa_decode_step_host_staging_bytes(4, 8, 2, 128, 16, 8, 100, 4, 0, 0, 0, 0)
+    # out + query (4*8*128*2 each), new K and V (4*2*128*2 each), slots, tables, lengths, 256-byte aligned
+    assert need == 2 * 8192 + 2 * 2048 + 256 + 256 + 256
+    assert lib.pa_decode_step_host_staging_bytes(4, 8, 2, 128, 16, 8, 100, 4, 0, 2, 0, 0) == 0  # no prefix
+    assert lib.pa_decode_step_host_staging_bytes(4, 8, 2, 128, 16, 8, 100, 4, 2, 2, 1, 0) > need
+
+    def step(out=buf, q=buf, nk=buf, T=4, pairs=None, n=0, B=4, S=0, pb=0, stg=buf, stg_bytes=1 << 30):
+        return lib.pa_decode_step_host(out, q, nk, buf, buf, T, pairs, n, buf, 8, buf, B, S, pb, 8, 2, 128, 16,
+                                       64, buf, buf, 100, f(0.1), 0, 1, stg, stg_bytes, None, None)
+    assert step(B=0) == -1
+    assert step(out=None) == -1
+    assert step(q=None) == -1
+    assert step(nk=None) == -1                  # new tokens without their keys
+    assert step(n=2) == -1                      # copy pairs without the list
+    assert step(S=2) == -1                      # groups without a shared prefix
+    assert step(stg=None) == -5
+    assert step(stg_bytes=need - 1) == -5
+    assert step(stg=p((1 << 20) + 16)) == -6    # staging not 256-byte aligned
+
+
 def test_block_manager_status_strings(lib):
     assert b"no free block" in lib.pa_status_string(-8) or b"exhausted" in lib.pa_status_string(-8)
 
