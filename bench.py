@@ -316,6 +316,10 @@ def main():
     ap.add_argument("--cpu-seqs", type=int, default=64, help="sequences in the CPU-baseline sample")
     ap.add_argument("--ref-seqs", type=int, default=2, help="sequences per reference-arm step")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--l2-flush", action="store_true",
+                    help="decode workloads: before every timed step write a 256 MB buffer (twice L2), then read "
+                         "another, so no line of the previous step survives and the written lines are evicted "
+                         "before the step; the step time is the sum of per-step events, which exclude the flush")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
 
@@ -401,6 +405,9 @@ def main():
     # ---- device-timed region: K steps, inputs resident in HBM
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
           for _ in range(args.steps)]
+    flush = torch.zeros((2, 256 << 20), dtype=torch.uint8, device=dev) if args.l2_flush else None
+    flush_sink = torch.zeros((), dtype=torch.int64, device=dev)
+    st_ev = [(torch.cuda.Event(enable_timing=True),) for _ in range(args.steps)] if flush is not None else None
     barrier(world)
     torch.cuda.synchronize()
     with ClockSampler(local) as clk:
@@ -408,6 +415,12 @@ def main():
         stop = torch.cuda.Event(enable_timing=True)
         start.record(stream)
         for i in range(args.steps):
+            if flush is not None:
+                # write 2x L2, then read another 2x L2 so the written lines are
+                # evicted (and written back) here, not inside the next step
+                flush[0].fill_(i & 0xff)
+                flush_sink.add_(flush[1].sum(dtype=torch.int64))
+                st_ev[i][0].record(stream)
             cow()
             pa.pa_reshape_and_cache(t["new_key"], t["new_value"], t["k_cache"], t["v_cache"], slots, d_err=err)
             ev[i][0].record(stream)
@@ -416,7 +429,11 @@ def main():
         stop.record(stream)
         torch.cuda.synchronize()
     barrier(world)
-    elapsed_ms = start.elapsed_time(stop)
+    if flush is not None:
+        # flushes fall between steps: the step time is the sum of its own events
+        elapsed_ms = sum(a.elapsed_time(b[1]) for a, b in zip((e[0] for e in st_ev), ev))
+    else:
+        elapsed_ms = start.elapsed_time(stop)
     decode_ms = [a.elapsed_time(b) for a, b in ev]
     elapsed_ms = max_over_ranks(elapsed_ms, world, dev)
 
@@ -485,7 +502,8 @@ def main():
                        "block_size": case.block_size, "context_lens": "uniform, see workload",
                        "max_context_len": case.max_context_len, "partition_tokens": part,
                        "pool_blocks": case.num_blocks,
-                       "l2": "inputs larger than L2: KV pool %.2f GB, %.2f GB read per step" % (
+                       "l2": ("L2 flushed before every step (256 MB written, then 256 MB read, outside the step's events); " if flush is not None
+                              else "") + "inputs larger than L2: KV pool %.2f GB, %.2f GB read per step" % (
                            2 * case.num_blocks * case.num_kv_heads * case.block_size * case.head_dim * 2 / 1e9,
                            case.kv_bytes() / 1e9),
                        "step": ("pa_copy_blocks + " if pairs is not None else "")
