@@ -21,6 +21,7 @@ reshape_and_cache_kernel(const uint4 *__restrict__ key, const uint4 *__restrict_
                          uint4 *__restrict__ k_cache, uint4 *__restrict__ v_cache,
                          const int64_t *__restrict__ slots, int num_tokens, int num_kv_heads,
                          int chunks_per_row, int block_size, long long pool_slots, int *d_err) {
+    pdl_trigger();  // the decode that follows may be scheduled; it waits for these writes
     const long long per_token = (long long)num_kv_heads * chunks_per_row;
     const long long total = per_token * num_tokens;
     for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < total;

@@ -260,6 +260,8 @@ __global__ void __launch_bounds__(NW * 32, decode_min_ctas<G>()) decode_kernel(c
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
+    pdl_wait();     // the kernel before this one on the stream (e.g. the cache write) has finished
+    pdl_trigger();  // the reduce may be scheduled once every CTA of this grid has started
 
     // ---- unit = (partition, sequence, kv head); partition-major order
     const int per_part = p.num_seqs * p.num_kv_heads;
@@ -533,6 +535,7 @@ __global__ void __launch_bounds__(NW * 32, decode_min_ctas<G>()) decode_kernel(c
 template <typename T, int D>
 __global__ void __launch_bounds__(128) decode_reduce_kernel(const DecodeParams p) {
     constexpr int VPL = D / 32;  // values per lane
+    pdl_wait();                  // the decode kernel's partials are complete and visible
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int pair = blockIdx.x * 4 + warp;
     if (pair >= p.num_seqs * p.num_heads) return;
@@ -595,12 +598,11 @@ int launch_decode_t(const DecodeParams &p, cudaStream_t stream) {
     const long long units = (long long)p.max_partitions * p.num_seqs * p.num_kv_heads;
     if (units <= 0) return PA_OK;
     if (units > 0x7fffffffLL) return PA_ERR_UNSUPPORTED;
-    kern<<<(unsigned)units, NW * 32, C::SMEM, stream>>>(p);
-    if (cudaPeekAtLastError() != cudaSuccess) return PA_ERR_CUDA;
+    if (launch_pdl(kern, dim3((unsigned)units), dim3(NW * 32), C::SMEM, stream, p) != cudaSuccess) return PA_ERR_CUDA;
     if (p.max_partitions > 1 && !p.force_partials) {
         const int pairs = p.num_seqs * p.num_heads;
-        decode_reduce_kernel<T, D><<<(pairs + 3) / 4, 128, 0, stream>>>(p);
-        if (cudaPeekAtLastError() != cudaSuccess) return PA_ERR_CUDA;
+        if (launch_pdl(decode_reduce_kernel<T, D>, dim3((pairs + 3) / 4), dim3(128), 0, stream, p) != cudaSuccess)
+            return PA_ERR_CUDA;
     }
     return PA_OK;
 }
@@ -609,10 +611,11 @@ template <typename T>
 int launch_reduce_dtype(int head_dim, const DecodeParams &p, cudaStream_t stream) {
     const int pairs = p.num_seqs * p.num_heads;
     if (pairs <= 0) return PA_OK;
-    if (head_dim == 128) decode_reduce_kernel<T, 128><<<(pairs + 3) / 4, 128, 0, stream>>>(p);
-    else if (head_dim == 64) decode_reduce_kernel<T, 64><<<(pairs + 3) / 4, 128, 0, stream>>>(p);
+    cudaError_t e;
+    if (head_dim == 128) e = launch_pdl(decode_reduce_kernel<T, 128>, dim3((pairs + 3) / 4), dim3(128), 0, stream, p);
+    else if (head_dim == 64) e = launch_pdl(decode_reduce_kernel<T, 64>, dim3((pairs + 3) / 4), dim3(128), 0, stream, p);
     else return PA_ERR_UNSUPPORTED;
-    return cudaPeekAtLastError() == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+    return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }
 
 template <typename T>

@@ -104,6 +104,9 @@ __global__ void __launch_bounds__(kThreads, 2)
     static_assert(kTK % BS == 0 && BS % 8 == 0 && 32 % kBPT == 0, "block_size");
     static_assert(G >= 1 && G <= kTG, "group");
 
+    pdl_wait();     // the kernel before this one on the stream (e.g. the cache write) has finished
+    pdl_trigger();  // the reduce may be scheduled once every CTA of this grid has started
+
     // ---- unit = (partition, sequence, kv head); partition-major order
     const int per_part = p.num_seqs * p.num_kv_heads;
     const int part = blockIdx.x / per_part;
@@ -500,8 +503,9 @@ int launch_tc_t(const DecodeParams &p, cudaStream_t stream) {
     const long long units = (long long)p.max_partitions * p.num_seqs * p.num_kv_heads;
     if (units <= 0) return PA_OK;
     if (units > 0x7fffffffLL) return PA_ERR_UNSUPPORTED;
-    kern<<<(unsigned)units, kThreads, kSmemAlloc, stream>>>(p, tmk, tmv);
-    return cudaPeekAtLastError() == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+    return launch_pdl(kern, dim3((unsigned)units), dim3(kThreads), kSmemAlloc, stream, p, tmk, tmv) == cudaSuccess
+               ? PA_OK
+               : PA_ERR_CUDA;
 }
 
 template <typename T, int G>

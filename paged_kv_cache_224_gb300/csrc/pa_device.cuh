@@ -5,7 +5,10 @@
 
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
+#include <cuda_runtime.h>
 #include <stdint.h>
+
+#include <utility>
 
 #include "../../include/pa.h"
 
@@ -134,6 +137,31 @@ __device__ __forceinline__ uint4 pack8(const float (&f)[8]) {
     u.z = Elem<T>::pack2(f[4], f[5]);
     u.w = Elem<T>::pack2(f[6], f[7]);
     return u;
+}
+
+// Programmatic dependent launch.  A kernel launched with programmatic stream
+// serialization (launch_pdl) may be scheduled before the kernel ahead of it
+// on the stream has finished; pdl_wait() blocks until that kernel has
+// completed and its writes are visible (a no-op for an ordinary launch), so
+// it comes before a kernel's first global access.  pdl_trigger() lets the
+// next such kernel be scheduled once every CTA of this one has called it.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                       Args &&...args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
 }
 
 __device__ __forceinline__ float fast_exp2(float x) {
