@@ -100,6 +100,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     volatile uint32_t *tmem_holder = reinterpret_cast<volatile uint32_t *>(o_done + kQT);
     static_assert((4 * kStages + 1 + 3 * kQT + 1) * 8 <= kSmemUsed - kOffBar, "barrier area");
 
+    pdl_wait();  // the kernel before this one on the stream (the chunk's cache write) has finished
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int kvh = blockIdx.y;
     const int rank = (int)cluster_rank();
@@ -454,13 +455,16 @@ int launch_tc_t(const PrefillParams &p, cudaStream_t stream) {
     cfg.blockDim = dim3(kThreads);
     cfg.dynamicSmemBytes = kSmemAlloc;
     cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = kCluster;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
+    // programmatic dependent launch: scheduled while the cache write drains
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = 2;
     return cudaLaunchKernelEx(&cfg, kern, p, tmk, tmv) == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }
 
