@@ -48,7 +48,8 @@ def load_peaks():
 
 def load_traffic(kernel_key: str, source: str = "pa_decode.cuh"):
     """Per-launch DRAM bytes of a kernel from the committed ncu summary, if
-    it was taken on the current kernel source."""
+    it was taken on the current kernel source (an entry lists the hash of
+    every source file it depends on, comma-separated)."""
     path = os.path.join(ROOT, "profiles", "traffic.txt")
     if not os.path.exists(path):
         return None
@@ -57,7 +58,7 @@ def load_traffic(kernel_key: str, source: str = "pa_decode.cuh"):
     sha = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
     for line in open(path):
         parts = line.split()
-        if len(parts) >= 3 and parts[0] == kernel_key and parts[1] == sha:
+        if len(parts) >= 3 and parts[0] == kernel_key and sha in parts[1].split(","):
             return float(parts[2])
     return None
 
@@ -446,10 +447,16 @@ def main():
     peak, peak_kind = load_peaks()
     dec_avg_ms = statistics.mean(decode_ms)
     dec_achieved = case.decode_bytes() / (dec_avg_ms / 1e3) / 1e9
-    kernel_key = f"decode_{case.name}"
     G = case.num_heads // case.num_kv_heads
     kname, ksrc = decode_kernel_of(G, case.head_dim)
-    traffic = load_traffic(kernel_key, ksrc)
+    if grouped:
+        # three kernels (prefix pass, tail pass, reduce): the traffic entry is
+        # their sum, valid while both decode sources are unchanged
+        pre_src = decode_kernel_of(G * case.group_size, case.head_dim)[1]
+        t_pre = load_traffic(f"decode_{case.name}_grouped", pre_src)
+        traffic = load_traffic(f"decode_{case.name}_grouped", ksrc) if t_pre is not None else None
+    else:
+        traffic = load_traffic(f"decode_{case.name}", ksrc)
 
     # ---- end to end through the C ABI's host-input step: every step copies
     # its inputs from pinned host memory (queries, new K/V, slots, copy pairs,
