@@ -234,15 +234,16 @@ def test_bad_table_entries_and_lengths_are_flagged_not_faulted():
     assert torch.isfinite(out2.float()).all()
 
 
-# Head groups of 8 at head_dim 128 run on the tensor cores (128-key tiles, one
-# 4-D copy per block): the same edge cases again for that kernel.
-TC_SHAPES = [(8, 2, "bf16"), (16, 2, "f16"), (32, 1, "bf16"), (64, 2, "f16"), (128, 1, "bf16")]
+# Head groups of 4 and 8 at head_dim 128 run on the tensor cores (128-key
+# tiles, one 4-D copy per block): the same edge cases again for that kernel.
+TC_SHAPES = [(8, 8, 2, "bf16"), (8, 16, 2, "f16"), (8, 32, 1, "bf16"), (8, 64, 2, "f16"), (8, 128, 1, "bf16"),
+             (4, 8, 2, "f16"), (4, 16, 3, "f16"), (4, 32, 2, "f16"), (4, 64, 1, "bf16"), (4, 128, 2, "f16")]
 
 
-@pytest.mark.parametrize("bs,Hkv,dtype", TC_SHAPES)
-def test_group8_tensor_core_shapes(bs, Hkv, dtype):
+@pytest.mark.parametrize("G,bs,Hkv,dtype", TC_SHAPES)
+def test_tensor_core_decode_shapes(G, bs, Hkv, dtype):
     lens = [1, 127, 128, 129, 255, 256, 257, bs + 1, 3 * bs + 5, 1000, 2049]
-    c = wl.make_decode_case(f"tc_bs{bs}", lens, 8 * Hkv, Hkv, 128, bs, dtype, seed=100 + bs)
+    c = wl.make_decode_case(f"tc_g{G}_bs{bs}", lens, G * Hkv, Hkv, 128, bs, dtype, seed=100 + bs + G)
     parity(c)
 
 
