@@ -361,3 +361,47 @@ def test_host_argument_errors_launch_nothing():
     with pytest.raises(pa.PAError):  # workspace too small for a split
         pa.pa_decode(out, t["query"], t["k_cache"], t["v_cache"], bt, lens, c.scale, 5000,
                      partition_tokens=16, workspace=torch.empty(16, dtype=torch.uint8, device=DEV))
+
+
+@pytest.mark.parametrize("G", [1, 4, 8])
+def test_decode_step_replays_from_a_cuda_graph(G):
+    # the step an engine captures once and replays every token: cache write,
+    # decode (programmatic dependent launches), split-K reduce
+    c = wl.make_decode_case(f"graph_g{G}", [1, 300, 2049, 700, 0], 2 * G, 2, 128, 16, "bf16", seed=70 + G)
+    t = c.materialize(DEV)
+    slots = torch.as_tensor(c.slot_mapping, device=DEV)
+    bt = torch.as_tensor(c.block_tables, device=DEV)
+    lens = torch.as_tensor(c.context_lens, device=DEV)
+    ws = pa.decode_workspace(t["query"], 2, 16, c.max_context_len, 256)
+    out = torch.empty_like(t["query"])
+    err = torch.zeros(1, dtype=torch.int32, device=DEV)
+
+    def step(o):
+        pa.pa_reshape_and_cache(t["new_key"], t["new_value"], t["k_cache"], t["v_cache"], slots, d_err=err)
+        pa.pa_decode(o, t["query"], t["k_cache"], t["v_cache"], bt, lens, c.scale, c.max_context_len,
+                     partition_tokens=256, workspace=ws, d_err=err)
+
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        step(out)  # eager warm-up outside the capture
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    ref = out.clone()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        step(out)
+    g = torch.Generator(device=DEV).manual_seed(9)
+    for i in range(3):
+        if i:
+            t["query"].copy_(torch.randn(t["query"].shape, generator=g, device=DEV).to(t["query"].dtype))
+        out.zero_()
+        graph.replay()
+        torch.cuda.synchronize()
+        eager = torch.empty_like(out)
+        step(eager)
+        torch.cuda.synchronize()
+        assert torch.equal(out, eager)
+        if i == 0:
+            assert torch.equal(out, ref)
+    assert int(err.item()) == 0
