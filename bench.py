@@ -201,6 +201,11 @@ def run_reference(args, world, rank):
     over a bounded sample of the workload's sequences."""
     if rank != 0:
         return
+    if args.workload in ("chunked_prefill", "prefill_batch", "mixed"):
+        if rank == 0:
+            print(json.dumps({"impl": "reference", "unavailable": "the reference arm times the CPU oracle's "
+                              "decode step; run it on a decode workload"}), flush=True)
+        return
     case = make_case(args.workload, 0)
     tensors = case.materialize("cpu")
     threads = os.cpu_count() or 1
@@ -304,6 +309,89 @@ def run_prefill_bench(args, world, rank, local, dev, stream):
         print(json.dumps(line), flush=True)
 
 
+def run_mixed_bench(args, world, rank, local, dev, stream):
+    """One continuous-batching step of a 64/8-head model: write the step's new
+    K/V (one decode token for each of 256 sequences, a 512-token prompt chunk),
+    then pa_mixed_step (the chunk's prefill and the decodes, concurrently).
+    The same step with the two calls one after the other is timed beside it."""
+    import paged_kv_cache_224_gb300 as pa
+    from paged_kv_cache_224_gb300 import workload as wl
+    case = wl.mixed_case(seed=1006 + rank)
+    t = case.materialize(dev)
+    slots = torch.as_tensor(case.slot_mapping, device=dev)
+    pbt = torch.as_tensor(case.prefill_tables, device=dev)
+    dbt = torch.as_tensor(case.decode_tables, device=dev)
+    lens = torch.as_tensor(case.context_lens, device=dev)
+    pout = torch.empty_like(t["prefill_query"])
+    dout = torch.empty_like(t["decode_query"])
+    ws = pa.decode_workspace(t["decode_query"], case.num_kv_heads, case.block_size, case.max_context_len,
+                             args.partition_tokens)
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    part = pa.pa_decode_partition_tokens(case.num_seqs, case.num_heads, case.num_kv_heads, case.block_size,
+                                         case.max_context_len, args.partition_tokens)
+    reduce_launch = 1 if -(-case.max_context_len // part) > 1 else 0
+
+    def write():
+        pa.pa_reshape_and_cache(t["new_key"], t["new_value"], t["k_cache"], t["v_cache"], slots, d_err=err)
+
+    def concurrent():
+        pa.pa_mixed_step(pout, t["prefill_query"], pbt, case.prefix_lens, case.chunk_lens, dout, t["decode_query"],
+                         dbt, lens, t["k_cache"], t["v_cache"], case.scale, case.max_context_len,
+                         partition_tokens=args.partition_tokens, workspace=ws, d_err=err)
+
+    def sequential():
+        pa.pa_prefill_batch(pout, t["prefill_query"], t["k_cache"], t["v_cache"], pbt, case.prefix_lens,
+                            case.chunk_lens, case.scale, d_err=err)
+        pa.pa_decode(dout, t["decode_query"], t["k_cache"], t["v_cache"], dbt, lens, case.scale,
+                     case.max_context_len, partition_tokens=args.partition_tokens, workspace=ws, d_err=err)
+
+    def timed(body):
+        for _ in range(args.warmup):
+            write()
+            body()
+        torch.cuda.synchronize()
+        barrier(world)
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        with ClockSampler(local) as clk:
+            a.record(stream)
+            for _ in range(args.steps):
+                write()
+                body()
+            b.record(stream)
+            torch.cuda.synchronize()
+        barrier(world)
+        return max_over_ranks(a.elapsed_time(b), world, dev) / args.steps, clk
+
+    ms_mixed, clk = timed(concurrent)
+    ms_seq, _ = timed(sequential)
+    if int(err.item()) != 0:
+        raise SystemExit(f"device error flags {int(err.item()):#x}")
+    peak, peak_kind = load_peaks()
+    dec_gbs = case.decode_bytes() / (ms_mixed / 1e3) / 1e9
+    if rank == 0:
+        line = {"metric": "mixed continuous-batching step (512-token prompt chunk + 256 decodes): ms per step",
+                "value": round(ms_mixed, 5), "unit": "ms", "n_gpus": world, "steps": args.steps,
+                "warmup": args.warmup, "ms_per_step": round(ms_mixed, 5), "higher_is_better": False,
+                "scaling": "weak", "vs_baseline": None, "dtype": case.dtype, "data": "synthetic",
+                "config": {"workload": case.name, "num_decode": case.num_seqs, "context_lens": "U{1..4096}",
+                           "prefix_len": case.prefix_lens.tolist(), "chunk_len": case.chunk_lens.tolist(),
+                           "num_heads": case.num_heads, "num_kv_heads": case.num_kv_heads,
+                           "head_dim": case.head_dim, "block_size": case.block_size, "partition_tokens": part,
+                           "step": "pa_reshape_and_cache (all new K/V) + pa_mixed_step",
+                           "l2": "inputs larger than L2: %.2f GB of decode KV per step" % (case.decode_bytes() / 1e9)},
+                "sequential_ms_per_step": round(ms_seq, 5),
+                "overlap_gain": round(ms_seq / ms_mixed - 1.0, 4),
+                "prefill_tflops_in_step": round(case.prefill_flops() / (ms_mixed / 1e3) / 1e12, 2),
+                "roofline": {"bound": "hbm", "achieved": round(dec_gbs, 2), "peak": peak, "unit": "GB/s",
+                             "frac": round(dec_gbs / peak, 4), "traffic": None,
+                             "kernel": "the decode half's KV streamed per step while the prompt chunk runs",
+                             "bytes_per_launch": case.decode_bytes(), "avg_ms": round(ms_mixed, 5),
+                             "peak_kind": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)"},
+                "gpu_launches": (3 + reduce_launch) * args.steps, "clocks": clk.summary()}
+        print(json.dumps(line), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -311,7 +399,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="llama_gqa", choices=["tiny", "llama_gqa", "opt13b_mha", "long_context", "long_context_bs32",
-                             "shared_prefix", "shared_prefix_grouped", "chunked_prefill", "prefill_batch"])
+                             "shared_prefix", "shared_prefix_grouped", "chunked_prefill", "prefill_batch", "mixed"])
     ap.add_argument("--partition-tokens", type=int, default=0)
     ap.add_argument("--e2e-steps", type=int, default=50)
     ap.add_argument("--cpu-seqs", type=int, default=64, help="sequences in the CPU-baseline sample")
@@ -341,8 +429,8 @@ def main():
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
     stream = torch.cuda.current_stream(dev)
-    if args.workload in ("chunked_prefill", "prefill_batch"):
-        run_prefill_bench(args, world, rank, local, dev, stream)
+    if args.workload in ("chunked_prefill", "prefill_batch", "mixed"):
+        (run_mixed_bench if args.workload == "mixed" else run_prefill_bench)(args, world, rank, local, dev, stream)
         if world > 1:
             import torch.distributed as dist
             dist.destroy_process_group()

@@ -268,6 +268,35 @@ PA_API int pa_decode_step_host(void *out_host, const void *query_host, const voi
                                void *staging, size_t staging_bytes, int *d_err, void *stream);
 
 /*
+ * pa_mixed_step -- one continuous-batching step over one pool: the prompt
+ * chunks of num_prefill sequences (exactly pa_prefill_batch) and one decode
+ * token for each of num_decode other sequences (exactly pa_decode), run
+ * concurrently.  The chunks' kernel goes first, on a high-priority stream the
+ * library forks from `stream` and joins back into it, so its CTAs are placed
+ * first; the decode streams KV over the SMs the chunks leave free (a prompt
+ * chunk's tensor-core CTAs need a whole SM's shared memory and tensor memory
+ * and cannot share one with decode CTAs) and takes every SM as the chunks
+ * finish.  The pages' chunked prefill, whose point is to batch prompt chunks
+ * with decodes ("vLLM PagedAttention chuyen sau" (locionic.com), "Chunked
+ * Prefill").  Both halves read the pool as it is when the call is reached
+ * on `stream`: write the step's new K/V first (pa_reshape_and_cache).
+ * Arguments as for pa_prefill_batch (prefill_*, prefix_lens, chunk_lens on
+ * the host) and pa_decode (decode_*, context_lens on the device, workspace),
+ * with the pool and the model shape shared.  A half with no sequences is
+ * skipped (no fork).  The fork stream and its two events are created on the
+ * first call on a device and kept; calls from several host threads are
+ * serialised around the fork.  Returns the first failing half's status
+ * (the other half may have been queued; the join is always queued).
+ */
+PA_API int pa_mixed_step(void *prefill_out, const void *prefill_query, const int32_t *prefill_block_tables,
+                         int prefill_max_blocks, const int *prefix_lens, const int *chunk_lens, int num_prefill,
+                         void *decode_out, const void *decode_query, const int32_t *decode_block_tables,
+                         int decode_max_blocks, const int32_t *context_lens, int num_decode, int max_context_len,
+                         int partition_tokens, void *workspace, size_t workspace_bytes, const void *k_cache,
+                         const void *v_cache, int num_heads, int num_kv_heads, int head_dim, int block_size,
+                         int num_blocks, float scale, pa_dtype dtype, int *d_err, void *stream);
+
+/*
  * pa_copy_blocks -- copy-on-write: for each pair (src, dst) of `pairs`
  * (int64 [num_pairs][2]), copy the whole K block and V block (all kv heads)
  * of src to dst, bit-exact.  A pair is skipped and PA_DEVERR_COPY_PAIR set

@@ -28,7 +28,8 @@ EXPORTED = ("pa_status_string", "pa_reshape_and_cache", "pa_decode_partition_tok
             "pa_decode_noalloc", "pa_decode_shared_prefix_workspace_bytes", "pa_decode_shared_prefix",
             "pa_bm_create", "pa_bm_destroy", "pa_bm_add_sequence", "pa_bm_fork", "pa_bm_append_token",
             "pa_bm_free_sequence", "pa_bm_block_table", "pa_bm_seq_len", "pa_bm_block_refcount",
-            "pa_bm_stats", "pa_prefill_batch", "pa_decode_step_host_staging_bytes", "pa_decode_step_host")
+            "pa_bm_stats", "pa_prefill_batch", "pa_decode_step_host_staging_bytes", "pa_decode_step_host",
+            "pa_mixed_step")
 PA_ERR_NO_BLOCKS = -8
 PA_ERR_SCRATCH_LIMIT = -7
 NOALLOC_SCRATCH_BYTES = 64 << 20
@@ -103,6 +104,9 @@ def lib() -> ctypes.CDLL:
         L.pa_decode_step_host.argtypes = [p, p, p, p, p, i, p, i, p, i, p, i, i, i, i, i, i, i, i, p, p, i,
                                           ctypes.c_float, i, i, p, sz, p, p]
         L.pa_decode_step_host.restype = i
+        L.pa_mixed_step.argtypes = [p, p, p, i, p, p, i, p, p, p, i, p, i, i, i, p, sz, p, p, i, i, i, i, i,
+                                    ctypes.c_float, i, p, p]
+        L.pa_mixed_step.restype = i
         _lib = L
     return _lib
 
@@ -305,6 +309,42 @@ def pa_decode_step_host(out, query, new_key, new_value, slot_mapping, block_tabl
         _ptr(k_cache), _ptr(v_cache), int(max_context_len), float(scale), int(partition_tokens), _dt(query),
         _ptr(staging), staging.numel() * staging.element_size(), _ptr(d_err), _stream(k_cache, stream))
     _check("pa_decode_step_host", rc)
+
+
+def pa_mixed_step(prefill_out, prefill_query, prefill_block_tables, prefix_lens, chunk_lens, decode_out,
+                  decode_query, decode_block_tables, context_lens, k_cache, v_cache, scale, max_context_len,
+                  partition_tokens=0, workspace=None, d_err=None, stream=None):
+    """One continuous-batching step: ``pa_prefill_batch`` over the prompt
+    chunks and ``pa_decode`` over the decoding sequences, run concurrently.
+    prefix_lens / chunk_lens are host int sequences; the rest as for those calls."""
+    _dev(prefill_out, prefill_query, prefill_block_tables, decode_out, decode_query, decode_block_tables,
+         context_lens, k_cache, v_cache, workspace, d_err)
+    for bt in (prefill_block_tables, decode_block_tables, context_lens):
+        if bt.dtype != torch.int32:
+            raise TypeError("block tables and context_lens must be int32")
+    NB, Hkv, bs, D = k_cache.shape
+    B, Hq, Dq = decode_query.shape
+    R, Hq2, Dq2 = prefill_query.shape
+    P = np.ascontiguousarray(np.asarray(prefix_lens, dtype=np.int32))
+    C = np.ascontiguousarray(np.asarray(chunk_lens, dtype=np.int32))
+    n = P.shape[0]
+    if Dq != D or Dq2 != D or Hq2 != Hq or decode_out.shape != decode_query.shape or \
+            prefill_out.shape != prefill_query.shape or C.shape != (n,) or int(C.sum()) != R or \
+            prefill_block_tables.shape[0] != n or decode_block_tables.shape[0] != B or context_lens.shape != (B,):
+        raise ValueError("shape mismatch")
+    if not (decode_query.dtype == prefill_query.dtype == decode_out.dtype == prefill_out.dtype == k_cache.dtype ==
+            v_cache.dtype):
+        raise TypeError("dtype mismatch")
+    if workspace is None:
+        workspace = decode_workspace(decode_query, Hkv, bs, max_context_len, partition_tokens)
+    rc = lib().pa_mixed_step(
+        _ptr(prefill_out), _ptr(prefill_query), _ptr(prefill_block_tables), prefill_block_tables.shape[1],
+        P.ctypes.data_as(ctypes.c_void_p), C.ctypes.data_as(ctypes.c_void_p), n, _ptr(decode_out),
+        _ptr(decode_query), _ptr(decode_block_tables), decode_block_tables.shape[1], _ptr(context_lens), B,
+        int(max_context_len), int(partition_tokens), _ptr(workspace), workspace.numel() * workspace.element_size(),
+        _ptr(k_cache), _ptr(v_cache), Hq, Hkv, D, bs, NB, float(scale), _dt(decode_query), _ptr(d_err),
+        _stream(k_cache, stream))
+    _check("pa_mixed_step", rc)
 
 
 def pa_copy_blocks(k_cache, v_cache, pairs, d_err=None, stream=None):

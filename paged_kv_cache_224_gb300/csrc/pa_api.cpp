@@ -5,6 +5,7 @@
 
 #include <algorithm>
 #include <cmath>
+#include <mutex>
 
 #include "../../include/pa.h"
 #include "pa_internal.h"
@@ -524,6 +525,85 @@ int pa_decode_step_host(void *out_host, const void *query_host, const void *new_
     if (rc != PA_OK) return rc;
     return cudaMemcpyAsync(out_host, d_out, qbytes, cudaMemcpyDeviceToHost, st) == cudaSuccess ? PA_OK
                                                                                                   : PA_ERR_CUDA;
+}
+
+}  // extern "C"
+
+// ---- one continuous-batching step: prompt chunks and decodes together ----------
+
+namespace {
+
+// A high-priority stream and two events per device, created on first use and
+// kept for the life of the process; the mutex keeps one call's fork, launches
+// and join together when several host threads use them.
+struct ForkStream {
+    cudaStream_t stream = nullptr;
+    cudaEvent_t fork = nullptr, join = nullptr;
+};
+std::mutex g_fork_mutex;
+ForkStream g_fork[64];
+
+int fork_stream(ForkStream **out) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return PA_ERR_CUDA;
+    ForkStream &f = g_fork[dev];
+    if (!f.stream) {
+        int least = 0, greatest = 0;
+        if (cudaDeviceGetStreamPriorityRange(&least, &greatest) != cudaSuccess ||
+            cudaEventCreateWithFlags(&f.fork, cudaEventDisableTiming) != cudaSuccess ||
+            cudaEventCreateWithFlags(&f.join, cudaEventDisableTiming) != cudaSuccess ||
+            cudaStreamCreateWithPriority(&f.stream, cudaStreamNonBlocking, greatest) != cudaSuccess)
+            return PA_ERR_CUDA;
+    }
+    *out = &f;
+    return PA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int pa_mixed_step(void *prefill_out, const void *prefill_query, const int32_t *prefill_block_tables,
+                  int prefill_max_blocks, const int *prefix_lens, const int *chunk_lens, int num_prefill,
+                  void *decode_out, const void *decode_query, const int32_t *decode_block_tables,
+                  int decode_max_blocks, const int32_t *context_lens, int num_decode, int max_context_len,
+                  int partition_tokens, void *workspace, size_t workspace_bytes, const void *k_cache,
+                  const void *v_cache, int num_heads, int num_kv_heads, int head_dim, int block_size, int num_blocks,
+                  float scale, pa_dtype dtype, int *d_err, void *stream) {
+    if (num_prefill < 0 || num_decode < 0) return PA_ERR_INVALID_ARG;
+    if (num_prefill == 0 || num_decode == 0) {
+        // one half only: no fork
+        int rc = pa_prefill_batch(prefill_out, prefill_query, k_cache, v_cache, prefill_block_tables,
+                                  num_prefill ? prefill_max_blocks : 1, prefix_lens, chunk_lens, num_prefill,
+                                  num_heads, num_kv_heads, head_dim, block_size, num_blocks, scale, dtype, d_err,
+                                  stream);
+        if (rc != PA_OK) return rc;
+        return pa_decode(decode_out, decode_query, k_cache, v_cache, decode_block_tables,
+                         num_decode ? decode_max_blocks : 1, context_lens, num_decode, num_heads, num_kv_heads,
+                         head_dim, block_size, num_blocks, max_context_len, scale, partition_tokens, dtype,
+                         workspace, workspace_bytes, d_err, stream);
+    }
+    std::lock_guard<std::mutex> guard(g_fork_mutex);
+    ForkStream *f = nullptr;
+    int rc = fork_stream(&f);
+    if (rc != PA_OK) return rc;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    // the prompt chunks go first, on the high-priority stream, so their CTAs
+    // are placed before the decode's; the decode streams KV on the SMs the
+    // chunks leave free, then on all of them
+    if (cudaEventRecord(f->fork, st) != cudaSuccess || cudaStreamWaitEvent(f->stream, f->fork, 0) != cudaSuccess)
+        return PA_ERR_CUDA;
+    const int rc_pf = pa_prefill_batch(prefill_out, prefill_query, k_cache, v_cache, prefill_block_tables,
+                                       prefill_max_blocks, prefix_lens, chunk_lens, num_prefill, num_heads,
+                                       num_kv_heads, head_dim, block_size, num_blocks, scale, dtype, d_err, f->stream);
+    const int rc_dec = pa_decode(decode_out, decode_query, k_cache, v_cache, decode_block_tables, decode_max_blocks,
+                                 context_lens, num_decode, num_heads, num_kv_heads, head_dim, block_size,
+                                 num_blocks, max_context_len, scale, partition_tokens, dtype, workspace,
+                                 workspace_bytes, d_err, stream);
+    // join even when a half failed, so the caller's stream never runs ahead of queued work
+    if (cudaEventRecord(f->join, f->stream) != cudaSuccess || cudaStreamWaitEvent(st, f->join, 0) != cudaSuccess)
+        return PA_ERR_CUDA;
+    return rc_pf != PA_OK ? rc_pf : rc_dec;
 }
 
 }  // extern "C"

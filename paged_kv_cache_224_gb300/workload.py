@@ -411,6 +411,82 @@ def make_prefill_batch_case(name: str, prefix_lens, chunk_lens, num_heads: int, 
                             np.zeros(0, np.int64), seed=seed)
 
 
+@dataclasses.dataclass
+class MixedCase:
+    """One continuous-batching step over one pool: prompt chunks of some
+    sequences (prefill) and one new token for each of the others (decode)."""
+    name: str
+    num_heads: int
+    num_kv_heads: int
+    head_dim: int
+    block_size: int
+    num_blocks: int
+    dtype: str
+    scale: float
+    context_lens: np.ndarray     # int32 [B] decode sequences, new token included
+    decode_tables: np.ndarray    # int32 [B][MB]
+    prefix_lens: np.ndarray      # int32 [n] prefill sequences
+    chunk_lens: np.ndarray       # int32 [n]
+    prefill_tables: np.ndarray   # int32 [n][MB]
+    slot_mapping: np.ndarray     # int64 [T]: the decode tokens (live sequences, in order), then the chunks' tokens
+    seed: int
+    tensors: dict = dataclasses.field(default_factory=dict)
+
+    @property
+    def num_seqs(self) -> int:
+        return int(self.context_lens.shape[0])
+
+    @property
+    def max_context_len(self) -> int:
+        return int(self.context_lens.max()) if self.num_seqs else 0
+
+    def decode_bytes(self) -> int:
+        el = 2
+        kv = int(self.context_lens.astype(np.int64).sum()) * 2 * self.num_kv_heads * self.head_dim * el
+        q = self.num_seqs * self.num_heads * self.head_dim * el
+        tables = sum(blocks_for(int(L), self.block_size) for L in self.context_lens) * 4
+        return kv + 2 * q + tables + 4 * self.num_seqs
+
+    def prefill_flops(self) -> int:
+        tot = sum(C * P + C * (C + 1) // 2 for P, C in zip(self.prefix_lens.tolist(), self.chunk_lens.tolist()))
+        return 4 * self.head_dim * tot * self.num_heads
+
+    def materialize(self, device="cpu") -> dict:
+        g = torch.Generator(device=device)
+        g.manual_seed(self.seed)
+        dt = TORCH_DTYPES[self.dtype]
+        Hq, Hkv, D = self.num_heads, self.num_kv_heads, self.head_dim
+        kc = torch.randn((self.num_blocks, Hkv, self.block_size, D), generator=g, device=device, dtype=dt)
+        vc = torch.randn((self.num_blocks, Hkv, self.block_size, D), generator=g, device=device, dtype=dt)
+        dq = torch.randn((self.num_seqs, Hq, D), generator=g, device=device, dtype=dt)
+        pq = torch.randn((int(self.chunk_lens.sum()), Hq, D), generator=g, device=device, dtype=dt)
+        T = int(self.slot_mapping.shape[0])
+        nk = torch.randn((T, Hkv, D), generator=g, device=device, dtype=dt)
+        nv = torch.randn((T, Hkv, D), generator=g, device=device, dtype=dt)
+        self.tensors = dict(k_cache=kc, v_cache=vc, decode_query=dq, prefill_query=pq, new_key=nk, new_value=nv)
+        return self.tensors
+
+
+def make_mixed_case(name: str, context_lens, prefix_lens, chunk_lens, num_heads: int, num_kv_heads: int,
+                    head_dim: int, block_size: int, dtype: str, seed: int, pool_factor: float = 1.25) -> MixedCase:
+    rng = np.random.Generator(np.random.PCG64(seed))
+    L = np.asarray(context_lens, dtype=np.int32)
+    P = np.asarray(prefix_lens, dtype=np.int32)
+    C = np.asarray(chunk_lens, dtype=np.int32)
+    tables, num_blocks = _scatter_tables(rng, [int(x) for x in L] + [int(p + c) for p, c in zip(P, C)],
+                                         block_size, None, pool_factor)
+    dt_, pt_ = tables[:len(L)], tables[len(L):]
+    live = [s for s in range(len(L)) if L[s] > 0]
+    slots = [_slots_of(dt_, live, [int(L[s]) - 1 for s in live], block_size)]
+    for i in range(len(P)):
+        pos = np.arange(P[i], P[i] + C[i], dtype=np.int64)
+        slots.append(pt_[i][pos // block_size].astype(np.int64) * block_size + pos % block_size)
+    return MixedCase(name=name, num_heads=num_heads, num_kv_heads=num_kv_heads, head_dim=head_dim,
+                     block_size=block_size, num_blocks=num_blocks, dtype=dtype, scale=1.0 / math.sqrt(head_dim),
+                     context_lens=L, decode_tables=dt_, prefix_lens=P, chunk_lens=C, prefill_tables=pt_,
+                     slot_mapping=np.concatenate(slots).astype(np.int64), seed=seed)
+
+
 # ---------------------------------------------------------------- workloads
 # The five workloads, named by what they are.  Seeds are 1000 + index.
 
@@ -466,6 +542,15 @@ def prefill_batch_case(seed: int = 1005) -> PrefillBatchCase:
     chunks = [512, 1024, 256, 2048, 512, 128, 1024, 512]
     prefixes = [int(x) for x in rng.integers(0, 16384, size=len(chunks))]
     return make_prefill_batch_case("prefill_batch8_bf16", prefixes, chunks, 64, 8, 128, 16, "bf16", seed=seed)
+
+
+def mixed_case(seed: int = 1006) -> MixedCase:
+    """A continuous-batching step of a 64/8-head model (D=128, bf16, bs 16):
+    one 512-token prompt chunk after an 8192-token prefix, and 256 decoding
+    sequences with L ~ U{1..4096}."""
+    rng = np.random.Generator(np.random.PCG64(seed + 7919))
+    lens = rng.integers(1, 4096 + 1, size=256)
+    return make_mixed_case("mixed_p8192_c512_b256_bf16", lens, [8192], [512], 64, 8, 128, 16, "bf16", seed=seed)
 
 
 def bits(t: torch.Tensor) -> np.ndarray:

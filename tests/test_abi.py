@@ -162,6 +162,23 @@ def test_host_step_rejects_bad_arguments_on_host(lib):
     assert step(stg=p((1 << 20) + 16)) == -6    # staging not 256-byte aligned
 
 
+def test_mixed_step_rejects_bad_arguments_on_host(lib):
+    p = ctypes.c_void_p
+    buf = p(1 << 20)
+    f = ctypes.c_float
+    pl = (ctypes.c_int * 2)(10, 0)
+    cl = (ctypes.c_int * 2)(4, 3)
+
+    def mixed(npf=2, ndec=3, Hq=8, Hkv=2, scale=0.1):
+        return lib.pa_mixed_step(buf, buf, buf, 4, pl, cl, npf, buf, buf, buf, 4, buf, ndec, 64, 0, buf, 1 << 30,
+                                 buf, buf, Hq, Hkv, 128, 16, 64, f(scale), 1, None, None)
+    assert mixed(npf=-1) == -1
+    assert mixed(ndec=-1) == -1
+    assert mixed(npf=0, ndec=0) == 0            # nothing to do, no CUDA call
+    assert mixed(npf=0, Hq=6, Hkv=4) == -1      # heads not a multiple of kv heads
+    assert mixed(ndec=0, scale=-1.0) == -3      # prefill half rejects a negative scale
+
+
 def test_block_manager_status_strings(lib):
     assert b"no free block" in lib.pa_status_string(-8) or b"exhausted" in lib.pa_status_string(-8)
 

@@ -1,0 +1,131 @@
+"""One continuous-batching step (pa_mixed_step): prompt chunks and decodes
+over one pool, run concurrently.
+
+The pages' chunked prefill batches prompt chunks with the decodes of other
+sequences (page "vLLM PagedAttention chuyen sau", section "Chunked
+Prefill").  The concurrent step must give, bit for bit, what the two calls
+give one after the other (the same kernels on the same inputs), and both
+halves must match the oracle.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import paged_kv_cache_224_gb300 as pa
+from paged_kv_cache_224_gb300 import workload as wl
+from tests.helpers import check_attention, to_f64
+
+pytestmark = pytest.mark.gpu
+DEV = torch.device("cuda:0") if torch.cuda.is_available() else None
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    import __graft_entry__ as g
+    g.build()
+
+
+def write_step_kv(case, t, err, slots=None):
+    if slots is None:
+        slots = torch.as_tensor(case.slot_mapping, device=DEV)
+    pa.pa_reshape_and_cache(t["new_key"], t["new_value"], t["k_cache"], t["v_cache"], slots, d_err=err)
+
+
+def device_args(case):
+    return (torch.as_tensor(case.prefill_tables, device=DEV), torch.as_tensor(case.decode_tables, device=DEV),
+            torch.as_tensor(case.context_lens, device=DEV))
+
+
+def mixed(case, t, err, pt=0):
+    pbt, dbt, lens = device_args(case)
+    pout = torch.full_like(t["prefill_query"], float("nan"))
+    dout = torch.full_like(t["decode_query"], float("nan"))
+    pa.pa_mixed_step(pout, t["prefill_query"], pbt, case.prefix_lens, case.chunk_lens, dout, t["decode_query"], dbt,
+                     lens, t["k_cache"], t["v_cache"], case.scale, case.max_context_len, partition_tokens=pt,
+                     d_err=err)
+    return pout, dout
+
+
+def separate(case, t, err, pt=0):
+    pbt, dbt, lens = device_args(case)
+    pout = torch.full_like(t["prefill_query"], float("nan"))
+    dout = torch.full_like(t["decode_query"], float("nan"))
+    pa.pa_prefill_batch(pout, t["prefill_query"], t["k_cache"], t["v_cache"], pbt, case.prefix_lens,
+                        case.chunk_lens, case.scale, d_err=err)
+    pa.pa_decode(dout, t["decode_query"], t["k_cache"], t["v_cache"], dbt, lens, case.scale, case.max_context_len,
+                 partition_tokens=pt, d_err=err)
+    return pout, dout
+
+
+@pytest.mark.parametrize("G,dtype", [(4, "bf16"), (8, "f16"), (1, "bf16")])
+def test_mixed_step_equals_the_two_calls_and_the_oracle(G, dtype):
+    c = wl.make_mixed_case(f"mixed_g{G}", [1, 300, 2049, 0, 700, 129], [40, 0, 333], [9, 17, 130], 2 * G, 2, 128,
+                           16, dtype, seed=80 + G)
+    t = c.materialize(DEV)
+    err = torch.zeros(1, dtype=torch.int32, device=DEV)
+    write_step_kv(c, t, err)
+    pm, dm = mixed(c, t, err, pt=256)
+    ps, ds = separate(c, t, err, pt=256)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    assert torch.equal(pm, ps) and torch.equal(dm, ds)
+    kc, vc = wl.bits(t["k_cache"]), wl.bits(t["v_cache"])
+    ref_d = oracle.decode(wl.bits(t["decode_query"]), kc, vc, c.decode_tables, c.context_lens, c.scale, dtype,
+                          num_threads=8)
+    check_attention(to_f64(dm), ref_d, dtype, "decode half")
+    q = wl.bits(t["prefill_query"])
+    row = 0
+    for i, (P, C) in enumerate(zip(c.prefix_lens.tolist(), c.chunk_lens.tolist())):
+        ref_p = oracle.prefill_chunk(q[row:row + C], kc, vc, c.prefill_tables[i], P, c.scale, dtype, num_threads=8)
+        check_attention(to_f64(pm[row:row + C]), ref_p, dtype, f"prefill seq {i}")
+        row += C
+
+
+def test_mixed_step_full_size_equals_the_two_calls():
+    c = wl.mixed_case()
+    t = c.materialize(DEV)
+    err = torch.zeros(1, dtype=torch.int32, device=DEV)
+    write_step_kv(c, t, err)
+    pm, dm = mixed(c, t, err)
+    ps, ds = separate(c, t, err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    assert torch.equal(pm, ps) and torch.equal(dm, ds)
+    assert torch.isfinite(pm.float()).all() and torch.isfinite(dm.float()).all()
+
+
+def test_mixed_step_replays_from_a_cuda_graph():
+    # the fork onto the library's stream and the join back must survive capture
+    c = wl.make_mixed_case("mixed_graph", [1, 300, 2049, 700], [100], [64], 8, 2, 128, 16, "bf16", seed=90)
+    t = c.materialize(DEV)
+    err = torch.zeros(1, dtype=torch.int32, device=DEV)
+    pbt, dbt, lens = device_args(c)
+    slots = torch.as_tensor(c.slot_mapping, device=DEV)  # no host copies inside the capture
+    ws = pa.decode_workspace(t["decode_query"], 2, 16, c.max_context_len, 256)
+    pout = torch.empty_like(t["prefill_query"])
+    dout = torch.empty_like(t["decode_query"])
+
+    def step():
+        write_step_kv(c, t, err, slots)
+        pa.pa_mixed_step(pout, t["prefill_query"], pbt, c.prefix_lens, c.chunk_lens, dout, t["decode_query"], dbt,
+                         lens, t["k_cache"], t["v_cache"], c.scale, c.max_context_len, partition_tokens=256,
+                         workspace=ws, d_err=err)
+
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        step()
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    ref_p, ref_d = pout.clone(), dout.clone()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        step()
+    pout.zero_()
+    dout.zero_()
+    graph.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(pout, ref_p) and torch.equal(dout, ref_d)
+    assert int(err.item()) == 0
+    assert not np.isnan(to_f64(pout)).any()
