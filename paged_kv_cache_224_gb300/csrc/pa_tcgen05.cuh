@@ -183,17 +183,18 @@ using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_
                                    CUtensorMapInterleave, CUtensorMapSwizzle, CUtensorMapL2promotion,
                                    CUtensorMapFloatOOBfill);
 
+// The driver's tensor-map encoder, looked up once (thread-safe static
+// initialisation); null when the driver does not provide it.
 inline EncodeTiledFn encode_fn() {
-    static EncodeTiledFn fn = nullptr;
-    if (!fn) {
+    static const EncodeTiledFn fn = []() -> EncodeTiledFn {
         void *ptr = nullptr;
         cudaDriverEntryPointQueryResult q;
         if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) !=
                 cudaSuccess ||
             q != cudaDriverEntryPointSuccess)
             return nullptr;
-        fn = reinterpret_cast<EncodeTiledFn>(ptr);
-    }
+        return reinterpret_cast<EncodeTiledFn>(ptr);
+    }();
     return fn;
 }
 
