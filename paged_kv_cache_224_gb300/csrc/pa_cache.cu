@@ -51,7 +51,8 @@ int launch_reshape_and_cache(const void *key, const void *value, void *k_cache, 
     const long long total = (long long)num_tokens * num_kv_heads * cpr;
     if (total == 0) return PA_OK;
     long long blocks = (total + 255) / 256;
-    if (blocks > 152LL * 64) blocks = 152LL * 64;  // grid-stride beyond 64 CTAs per SM
+    const long long cap = (long long)sm_count() * 64;  // grid-stride beyond 64 CTAs per SM
+    if (blocks > cap) blocks = cap;
     reshape_and_cache_kernel<<<(unsigned)blocks, 256, 0, stream>>>(
         static_cast<const uint4 *>(key), static_cast<const uint4 *>(value),
         static_cast<uint4 *>(k_cache), static_cast<uint4 *>(v_cache), slots, num_tokens,

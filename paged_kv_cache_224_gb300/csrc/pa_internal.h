@@ -11,6 +11,19 @@
 
 namespace pa {
 
+// Streaming multiprocessors of the current device, queried once per device
+// (152 on a GB300; also the answer when no device is present).
+inline int sm_count() {
+    static std::atomic<int> cached[64];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 152;
+    int n = cached[dev].load(std::memory_order_relaxed);
+    if (n > 0) return n;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) return 152;
+    cached[dev].store(n, std::memory_order_relaxed);
+    return n;
+}
+
 // Raise a kernel's dynamic shared-memory limit once per device (the attribute
 // is per device; `done` is the caller's per-kernel record of devices set).
 template <typename Kernel>
