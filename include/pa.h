@@ -297,6 +297,19 @@ PA_API int pa_mixed_step(void *prefill_out, const void *prefill_query, const int
                          int num_blocks, float scale, pa_dtype dtype, int *d_err, void *stream);
 
 /*
+ * Failure detection.  Every wait inside the kernels (on TMA copies, MMA
+ * completions, other warps) is bounded: after pa_bounded_wait_polls() polls
+ * it gives up, ORs PA_DEVERR_TIMEOUT into *d_err and lets the kernel finish,
+ * so a stuck pipeline is reported and the context stays usable.
+ * pa_selftest_bounded_wait runs that same wait, with max_polls polls, on a
+ * barrier nothing ever arrives on: it must set PA_DEVERR_TIMEOUT in *d_err
+ * (device int) and, if d_cycles is not NULL, write the SM clock cycles the
+ * wait took to *d_cycles (device long long).  Asynchronous on `stream`.
+ */
+PA_API int pa_bounded_wait_polls(void);
+PA_API int pa_selftest_bounded_wait(int max_polls, int *d_err, long long *d_cycles, void *stream);
+
+/*
  * pa_copy_blocks -- copy-on-write: for each pair (src, dst) of `pairs`
  * (int64 [num_pairs][2]), copy the whole K block and V block (all kv heads)
  * of src to dst, bit-exact.  A pair is skipped and PA_DEVERR_COPY_PAIR set

@@ -29,7 +29,7 @@ EXPORTED = ("pa_status_string", "pa_reshape_and_cache", "pa_decode_partition_tok
             "pa_bm_create", "pa_bm_destroy", "pa_bm_add_sequence", "pa_bm_fork", "pa_bm_append_token",
             "pa_bm_free_sequence", "pa_bm_block_table", "pa_bm_seq_len", "pa_bm_block_refcount",
             "pa_bm_stats", "pa_prefill_batch", "pa_decode_step_host_staging_bytes", "pa_decode_step_host",
-            "pa_mixed_step")
+            "pa_mixed_step", "pa_bounded_wait_polls", "pa_selftest_bounded_wait")
 PA_ERR_NO_BLOCKS = -8
 PA_ERR_SCRATCH_LIMIT = -7
 NOALLOC_SCRATCH_BYTES = 64 << 20
@@ -107,6 +107,10 @@ def lib() -> ctypes.CDLL:
         L.pa_mixed_step.argtypes = [p, p, p, i, p, p, i, p, p, p, i, p, i, i, i, p, sz, p, p, i, i, i, i, i,
                                     ctypes.c_float, i, p, p]
         L.pa_mixed_step.restype = i
+        L.pa_bounded_wait_polls.argtypes = []
+        L.pa_bounded_wait_polls.restype = i
+        L.pa_selftest_bounded_wait.argtypes = [i, p, p, p]
+        L.pa_selftest_bounded_wait.restype = i
         _lib = L
     return _lib
 
@@ -345,6 +349,14 @@ def pa_mixed_step(prefill_out, prefill_query, prefill_block_tables, prefix_lens,
         _ptr(k_cache), _ptr(v_cache), Hq, Hkv, D, bs, NB, float(scale), _dt(decode_query), _ptr(d_err),
         _stream(k_cache, stream))
     _check("pa_mixed_step", rc)
+
+
+def pa_selftest_bounded_wait(max_polls, d_err, d_cycles=None, stream=None):
+    """Run the kernels' bounded wait on a barrier nothing arrives on; it must
+    give up after ``max_polls`` polls and set the timeout bit in ``d_err``."""
+    _dev(d_err, d_cycles)
+    rc = lib().pa_selftest_bounded_wait(int(max_polls), _ptr(d_err), _ptr(d_cycles), _stream(d_err, stream))
+    _check("pa_selftest_bounded_wait", rc)
 
 
 def pa_copy_blocks(k_cache, v_cache, pairs, d_err=None, stream=None):

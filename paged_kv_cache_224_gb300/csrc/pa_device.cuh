@@ -17,9 +17,11 @@ namespace pa {
 constexpr unsigned kFull = 0xffffffffu;
 
 // Upper bound on mbarrier polls before a wait gives up and flags
-// PA_DEVERR_TIMEOUT.  Each try_wait may itself suspend for a while, so this
-// is on the order of a second -- far beyond any legitimate copy latency.
-constexpr uint32_t kMaxPolls = 1u << 20;
+// PA_DEVERR_TIMEOUT.  A poll that finds the phase incomplete suspends for a
+// while (about 7800 SM cycles on a GB300, measured with the self-test), so
+// 2^18 polls is about one second -- orders of magnitude above any legitimate
+// copy or pipeline latency.
+constexpr uint32_t kMaxPolls = 1u << 18;
 
 __device__ __forceinline__ uint32_t smem_addr(const void *p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -60,8 +62,8 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
 
 // Bounded wait for the phase with the given parity.  Returns false (after
 // kMaxPolls polls) if the phase never completed.
-__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity) {
-    for (uint32_t i = 0; i < kMaxPolls; ++i)
+__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, uint32_t max_polls = kMaxPolls) {
+    for (uint32_t i = 0; i < max_polls; ++i)
         if (mbar_try_wait(bar, parity)) return true;
     return false;
 }
