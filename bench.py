@@ -443,6 +443,8 @@ def main():
     if tensors_host_copy_needed:
         # the oracle reads the pre-step pool: take its sample before any kernel runs
         cpu_sample = cpu_oracle_sample(case, t, args.cpu_seqs, os.cpu_count() or 1)
+        cpu_seqs_1 = max(4, args.cpu_seqs // 8)
+        cpu_sample_1 = cpu_oracle_sample(case, t, cpu_seqs_1, 1)
 
     slots = torch.as_tensor(case.slot_mapping, device=dev)
     bt = torch.as_tensor(case.block_tables, device=dev)
@@ -628,7 +630,10 @@ def main():
             line["cpu_baseline"] = {"value": round(b / dt / 1e9, 4), "unit": "GB/s",
                                     "cores": os.cpu_count() or 1, "kind": "oracle",
                                     "sample": f"first {min(args.cpu_seqs, case.num_seqs)} of {case.num_seqs} "
-                                              f"sequences of {case.name}: cache write + decode, fp64"}
+                                              f"sequences of {case.name}: cache write + decode, fp64",
+                                    "single_thread": {
+                                        "value": round(cpu_sample_1[1] / cpu_sample_1[0] / 1e9, 4), "cores": 1,
+                                        "sample": f"first {min(cpu_seqs_1, case.num_seqs)} sequences, same step"}}
         print(json.dumps(line), flush=True)
     if world > 1:
         import torch.distributed as dist
