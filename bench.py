@@ -65,7 +65,7 @@ def load_traffic(kernel_key: str, source: str = "pa_decode.cuh"):
 
 def decode_kernel_of(group: int, head_dim: int):
     """The decode kernel the library runs for a head group, and its source file."""
-    if group in (4, 8) and head_dim == 128:
+    if group == 8 and head_dim == 128:
         return "decode_tc_kernel", "pa_decode_tc.cu"
     return "decode_kernel", "pa_decode.cuh"
 

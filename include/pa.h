@@ -124,9 +124,9 @@ PA_API size_t pa_decode_workspace_bytes(int num_seqs, int num_heads, int num_kv_
  *   2. gather K and V rows from those blocks,
  *   3. out[s][h] = sum_j softmax_j(scale * q[s][h] . K_j) V_j,
  * accumulated in fp32 and rounded once to dtype (round to nearest even).
- * Groups of 4 and 8 at head_dim 128 run on the tensor cores: the products
+ * Groups of 8 at head_dim 128 run on the tensor cores: the products
  * accumulate in fp32, and the softmax weights are rounded to dtype before
- * they multiply V (groups of 1 and 2, and head_dim 64, keep them in fp32).
+ * they multiply V (smaller groups, and head_dim 64, keep them in fp32).
  *
  *   out            [num_seqs][num_heads][head_dim] dtype (written)
  *   query          [num_seqs][num_heads][head_dim] dtype

@@ -43,15 +43,15 @@ int launch_decode_reduce(pa_dtype dt, int head_dim, const DecodeParams &p, cudaS
 // is estimated from the host-side arguments only (every sequence's length is
 // on the device): num_seqs * max_context_len / 2 tokens per kv head, spread
 // over the GPU's SMs (152) x the resident CTAs of the kernel that runs (3 for
-// the CUDA-core kernel at groups up to 2; 2 for groups of 4 and 8, which run
-// on the tensor cores at head_dim 128 and hold 2 CTAs per SM on the CUDA
-// cores at group 8).  The result is the power of two nearest that estimate
-// within [256, 4096] (a multiple of block_size).  Measured on the decode
-// workloads: LLaMA GQA picks 2048 (102% of the measured copy peak against 94%
-// at 512), long context 2048, OPT MHA 512, the shared-prefix batch 2048.
+// the CUDA-core kernel at groups up to 4; 2 for groups of 8, which run on the
+// tensor cores at head_dim 128 and hold 2 CTAs per SM on the CUDA cores).
+// The result is the power of two nearest that estimate within [256, 4096] (a
+// multiple of block_size).  Measured on the decode workloads: LLaMA GQA picks
+// 1024 (98.8% of HBM peak against 96.5% at 512), long context 2048, OPT MHA
+// 512, the shared-prefix batch 2048 (1.84x against 1.55x logical).
 int auto_partition_tokens(int num_seqs, int num_heads, int num_kv_heads, int block_size, int max_context_len) {
     const int group = num_heads / num_kv_heads;
-    const double slots = (double)pa::sm_count() * (group <= 2 ? 3 : 2);
+    const double slots = (double)pa::sm_count() * (group <= 4 ? 3 : 2);
     const double per_part = (double)num_seqs * max_context_len * 0.5 * num_kv_heads / slots / 8.0;
     int pt = 256;
     while (pt < 4096 && per_part > pt * 1.41421356) pt *= 2;

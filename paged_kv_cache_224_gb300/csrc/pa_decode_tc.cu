@@ -1,14 +1,14 @@
-// Paged decode attention for head groups of 4 and 8 on the tensor cores
-// (tcgen05).
+// Paged decode attention for head groups of 8 on the tensor cores (tcgen05).
 //
 // Same operation and work units as the CUDA-core decode kernel (the three
 // steps of the page "vLLM PagedAttention chuyen sau" (locionic.com), section
 // "Co che PagedAttention": look up each logical block in the block table,
-// gather its K/V rows, attend), for the shapes where CUDA cores run short of
-// issue slots: with G query heads per kv head every K/V byte feeds G dot
-// products, and the group's scores and weighted sums are small dense
-// contractions.  Keys are the MMA's M dimension, so nothing is padded along
-// the long axis:
+// gather its K/V rows, attend), for the shape where the CUDA cores run out of
+// issue slots well below the HBM bound: with 8 query heads per kv head every
+// K/V byte feeds 8 dot products and 8 weighted sums, and the group's scores
+// and weighted sums are dense contractions.  (Smaller groups are HBM-bound on
+// the CUDA cores and stay there; the kernel is written for any G up to 8.)
+// Keys are the MMA's M dimension, so nothing is padded along the long axis:
 //   S^T[128 keys][16] = K[128 keys][128 dims] . Q^T    (Q: the G heads, zero rows up to N = 16)
 //   O^T[128 dims][16] += V^T[128 dims][128 keys] . P^T (V read in place, MN-major)
 // fp32 accumulators in tensor memory; P is rounded to the input type.
@@ -523,7 +523,6 @@ int launch_tc_group(int block_size, const DecodeParams &p, cudaStream_t stream) 
 template <typename T>
 int launch_tc_dtype(int block_size, int group, const DecodeParams &p, cudaStream_t stream) {
     switch (group) {
-        case 4: return launch_tc_group<T, 4>(block_size, p, stream);
         case 8: return launch_tc_group<T, 8>(block_size, p, stream);
         default: return PA_ERR_UNSUPPORTED;
     }

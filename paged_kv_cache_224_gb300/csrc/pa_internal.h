@@ -96,10 +96,11 @@ int auto_partition_tokens(int num_seqs, int num_heads, int num_kv_heads, int blo
 // the shape) or PA_ERR_CUDA (launch / attribute failure).
 int launch_decode(pa_dtype dt, int head_dim, int block_size, int group, const DecodeParams &p,
                   cudaStream_t stream);
-// Groups whose decode runs on the tensor cores at head_dim 128.  Groups of 1
-// and 2 stay on the CUDA cores, which reach the HBM bound there with three
-// CTAs per SM (and reuse shared prefix blocks through L2 better).
-inline bool decode_tc_group(int group) { return group == 4 || group == 8; }
+// Groups whose decode runs on the tensor cores at head_dim 128: only groups
+// of 8, where every K/V byte feeds 8 dot products and 8 weighted sums and the
+// CUDA-core kernel runs out of issue slots well below the HBM bound.  Groups
+// of 1, 2 and 4 are HBM-bound on the CUDA cores and stay there.
+inline bool decode_tc_group(int group) { return group == 8; }
 // Decode on the tensor cores (the decode kernel only; the caller launches the
 // reduce).  PA_ERR_UNSUPPORTED for any other shape, or when the driver
 // refuses the kernel's tensor maps.

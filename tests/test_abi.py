@@ -49,7 +49,7 @@ def test_workspace_and_partition_rules(lib):
     # every sequence fits one partition -> no workspace
     assert pa.pa_decode_workspace_bytes(4, 4, 4, 64, 16, 64, 0) == 0
     # the automatic length on the decode workloads: LLaMA GQA, long context, OPT MHA
-    assert pa.pa_decode_partition_tokens(256, 32, 8, 16, 4096, 0) == 2048
+    assert pa.pa_decode_partition_tokens(256, 32, 8, 16, 4096, 0) == 1024
     assert pa.pa_decode_partition_tokens(8, 64, 8, 16, 131072, 0) == 2048
     assert pa.pa_decode_partition_tokens(64, 40, 40, 16, 2048, 0) == 512
     # few, short sequences: the shortest partitions; huge batches: the longest
@@ -57,7 +57,7 @@ def test_workspace_and_partition_rules(lib):
     assert pa.pa_decode_partition_tokens(4096, 64, 8, 16, 32768, 0) == 4096
     assert pa.pa_decode_partition_tokens(1, 8, 8, 128, 16, 0) == 256
     n = pa.pa_decode_workspace_bytes(256, 32, 8, 128, 16, 4096, 0)
-    parts = 2
+    parts = 4
     assert n >= 256 * 32 * parts * (128 + 2) * 4
     # explicit partitions must be multiples of block_size
     assert pa.pa_decode_partition_tokens(4, 4, 4, 16, 100, 24) == 0

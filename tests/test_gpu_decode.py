@@ -234,8 +234,9 @@ def test_bad_table_entries_and_lengths_are_flagged_not_faulted():
     assert torch.isfinite(out2.float()).all()
 
 
-# Head groups of 4 and 8 at head_dim 128 run on the tensor cores (128-key
-# tiles, one 4-D copy per block): the same edge cases again for that kernel.
+# Head groups of 8 at head_dim 128 run on the tensor cores (128-key tiles,
+# one 4-D copy per block): the same edge cases again for that kernel, and for
+# groups of 4 (CUDA cores) at every block size.
 TC_SHAPES = [(8, 8, 2, "bf16"), (8, 16, 2, "f16"), (8, 32, 1, "bf16"), (8, 64, 2, "f16"), (8, 128, 1, "bf16"),
              (4, 8, 2, "f16"), (4, 16, 3, "f16"), (4, 32, 2, "f16"), (4, 64, 1, "bf16"), (4, 128, 2, "f16")]
 
