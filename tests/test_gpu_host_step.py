@@ -90,3 +90,23 @@ def test_host_step_shared_prefix_with_copy_on_write():
     assert torch.equal(out_host, out_dev.cpu())
     assert torch.equal(t["k_cache"], t_dev["k_cache"]) and torch.equal(t["v_cache"], t_dev["v_cache"])
     assert np.isfinite(to_f64(out_host)).all()
+
+
+def test_host_step_without_new_tokens_or_pairs():
+    # a step that only attends (the new tokens were written earlier): no cache
+    # write is queued, and the output equals the device-pointer decode
+    c = wl.make_decode_case("host_noop", [1, 300, 700], 8, 2, 128, 16, "bf16", seed=66)
+    t = c.materialize(DEV)
+    ref = torch.full_like(t["query"], float("nan"))
+    pa.pa_decode(ref, t["query"], t["k_cache"], t["v_cache"], torch.as_tensor(c.block_tables, device=DEV),
+                 torch.as_tensor(c.context_lens, device=DEV), c.scale, c.max_context_len)
+    before = t["k_cache"].clone()
+    out = torch.full(tuple(t["query"].shape), float("nan"), dtype=t["query"].dtype).pin_memory()
+    empty_kv = t["new_key"][:0].cpu().pin_memory()
+    pa.pa_decode_step_host(out, t["query"].cpu().pin_memory(), empty_kv, empty_kv,
+                           torch.zeros(0, dtype=torch.int64).pin_memory(),
+                           torch.as_tensor(c.block_tables).pin_memory(), torch.as_tensor(c.context_lens).pin_memory(),
+                           t["k_cache"], t["v_cache"], c.scale, c.max_context_len)
+    torch.cuda.synchronize()
+    assert torch.equal(out, ref.cpu())
+    assert torch.equal(t["k_cache"], before)

@@ -129,3 +129,26 @@ def test_mixed_step_replays_from_a_cuda_graph():
     assert torch.equal(pout, ref_p) and torch.equal(dout, ref_d)
     assert int(err.item()) == 0
     assert not np.isnan(to_f64(pout)).any()
+
+
+def test_mixed_step_with_one_half_empty_runs_that_half_alone():
+    c = wl.make_mixed_case("mixed_one", [1, 300, 700], [50], [20], 16, 2, 128, 16, "bf16", seed=95)
+    t = c.materialize(DEV)
+    err = torch.zeros(1, dtype=torch.int32, device=DEV)
+    write_step_kv(c, t, err)
+    pbt, dbt, lens = device_args(c)
+    ps, ds = separate(c, t, err)
+    # decode only: an empty prompt-chunk list
+    dout = torch.full_like(t["decode_query"], float("nan"))
+    empty_q = t["prefill_query"][:0]
+    pa.pa_mixed_step(empty_q.clone(), empty_q, pbt[:0], np.zeros(0, np.int32), np.zeros(0, np.int32), dout,
+                     t["decode_query"], dbt, lens, t["k_cache"], t["v_cache"], c.scale, c.max_context_len,
+                     d_err=err)
+    # prefill only: no decoding sequences
+    pout = torch.full_like(t["prefill_query"], float("nan"))
+    empty_d = t["decode_query"][:0]
+    pa.pa_mixed_step(pout, t["prefill_query"], pbt, c.prefix_lens, c.chunk_lens, empty_d.clone(), empty_d, dbt[:0],
+                     lens[:0], t["k_cache"], t["v_cache"], c.scale, 1, d_err=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    assert torch.equal(dout, ds) and torch.equal(pout, ps)
