@@ -406,3 +406,12 @@ def test_decode_step_replays_from_a_cuda_graph(G):
         if i == 0:
             assert torch.equal(out, ref)
     assert int(err.item()) == 0
+
+
+@pytest.mark.parametrize("G,dtype", [(1, "f16"), (8, "bf16")])
+def test_hundreds_of_partitions_merge_in_the_reduce(G, dtype):
+    # one long sequence in 128-token partitions: the log-sum-exp reduce merges
+    # hundreds of partials per head (more than a warp has lanes), beside
+    # short sequences that fit one partition and write their output directly
+    c = wl.make_decode_case(f"many_parts_g{G}", [60000, 5, 129, 3000], 2 * G, 2, 128, 16, dtype, seed=140 + G)
+    parity(c, partition_tokens=128)
