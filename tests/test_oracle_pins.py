@@ -255,6 +255,22 @@ def test_physical_permutation_invariance(oracle_mod):
     assert np.array_equal(a, b)
 
 
+@pytest.mark.parametrize("G", [2, 4, 8])
+def test_grouped_heads_equal_mha_with_kv_heads_repeated(oracle_mod, G):
+    # the textbook reduction: query head h of a group-of-G model attends to kv
+    # head h // G, i.e. to the same rows as an MHA model whose pool holds
+    # each kv head G times in a row (a wrong head map, e.g. h % Hkv, breaks it)
+    Hkv = 2
+    c = wl.make_decode_case("gqa", [30, 50, 17, 64], G * Hkv, Hkv, 64, 16, "bf16", seed=17 + G)
+    t = c.materialize("cpu")
+    q, kc, vc = wl.bits(t["query"]), wl.bits(t["k_cache"]), wl.bits(t["v_cache"])
+    gqa = oracle_mod.decode(q, kc, vc, c.block_tables, c.context_lens, c.scale, c.dtype)
+    kc_rep = np.ascontiguousarray(np.repeat(kc, G, axis=1))   # [NB][Hkv*G][bs][D]
+    vc_rep = np.ascontiguousarray(np.repeat(vc, G, axis=1))
+    mha = oracle_mod.decode(q, kc_rep, vc_rep, c.block_tables, c.context_lens, c.scale, c.dtype)
+    assert np.array_equal(gqa, mha)
+
+
 def test_shared_prefix_equals_private_copies(oracle_mod):
     c = wl.make_shared_prefix_case("t", num_prompts=2, samples=3, prefix_len=40, max_tail=20,
                                    num_heads=2, head_dim=64, block_size=16, dtype="f16", seed=4)
