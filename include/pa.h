@@ -125,8 +125,10 @@ PA_API size_t pa_decode_workspace_bytes(int num_seqs, int num_heads, int num_kv_
  *   3. out[s][h] = sum_j softmax_j(scale * q[s][h] . K_j) V_j,
  * accumulated in fp32 and rounded once to dtype (round to nearest even).
  * Groups of 8 at head_dim 128 run on the tensor cores: the products
- * accumulate in fp32, and the softmax weights are rounded to dtype before
- * they multiply V (smaller groups, and head_dim 64, keep them in fp32).
+ * accumulate in fp32, and each softmax weight enters the weighted sum as
+ * two dtype values (its rounding and the rounded residual), which keeps it
+ * to about twice dtype's precision (smaller groups, and head_dim 64, keep
+ * the weights in fp32).
  *
  *   out            [num_seqs][num_heads][head_dim] dtype (written)
  *   query          [num_seqs][num_heads][head_dim] dtype

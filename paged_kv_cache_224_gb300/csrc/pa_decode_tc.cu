@@ -11,7 +11,9 @@
 // Keys are the MMA's M dimension, so nothing is padded along the long axis:
 //   S^T[128 keys][16] = K[128 keys][128 dims] . Q^T    (Q: the G heads, zero rows up to N = 16)
 //   O^T[128 dims][16] += V^T[128 dims][128 keys] . P^T (V read in place, MN-major)
-// fp32 accumulators in tensor memory; P is rounded to the input type.
+// fp32 accumulators in tensor memory.  P enters the MMA as two 16-bit rows
+// per head, its rounding and the rounding residual, in the N padding (rows 8-15),
+// so the PV product keeps P to about twice the input type's precision.
 //
 // One CTA = one unit (sequence, kv head, partition), 128-key tiles:
 //   warp 0    TMA producer: one 4-D tensor copy per (block, K or V) from the
@@ -314,7 +316,7 @@ __global__ void __launch_bounds__(kThreads, 2)
         const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
         const float csc = p.scale_log2;
         {
-            // Q^T rows 0..G-1 = the group's query heads, the rest zero; P^T rows 8-15 zero
+            // Q^T rows 0..G-1 = the group's query heads, the rest zero
             const uint4 z = make_uint4(0, 0, 0, 0);
             const int h = t >> 4, c = t & 15;
             const uint4 q = h < G ? *reinterpret_cast<const uint4 *>(static_cast<const T *>(p.query) +
@@ -322,13 +324,6 @@ __global__ void __launch_bounds__(kThreads, 2)
                                   : z;
             sts128(sb + kOffQ + (c >> 3) * 2048 + h * 128 + (((c & 7) ^ h) << 4), q);
             sts128(sb + kOffQ + (c >> 3) * 2048 + (8 + h) * 128 + (((c & 7) ^ h) << 4), z);
-#pragma unroll
-            for (int r = 0; r < 2; ++r) {
-                const int idx = t + r * 128;  // [buffer][key half][row 8-15][16-byte chunk]
-                sts128(sb + kOffP + (idx >> 7) * 4096 + ((idx >> 6) & 1) * 2048 + (8 + ((idx >> 3) & 7)) * 128 +
-                           (idx & 7) * 16,
-                       z);
-            }
             asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
             mbar_arrive1(q_full);
         }
@@ -384,15 +379,16 @@ __global__ void __launch_bounds__(kThreads, 2)
                 // O must hold the PV of tile j-1 before it is scaled
                 wait_or_flag(&pv_done[(j - 1) & 1], (uint32_t)((j - 1) >> 1) & 1u, p.d_err);
                 tc_fence_after();
-                float o[kTG];
-                tmem_ld8(tmem + lane_off + kColO, o);
+                float o[2 * kTG];  // the P_hi and P_lo columns of each head
+                tmem_ld16(tmem + lane_off + kColO, o);
                 tmem_wait_ld();
 #pragma unroll
                 for (int h = 0; h < kTG; ++h) {
                     o[h] *= alpha[h];
+                    o[kTG + h] *= alpha[h];
                     l_part[h] *= alpha[h];
                 }
-                tmem_st8(tmem + lane_off + kColO, o);
+                tmem_st16(tmem + lane_off + kColO, o);
             }
             float pr[kTG];
 #pragma unroll
@@ -403,13 +399,25 @@ __global__ void __launch_bounds__(kThreads, 2)
             // P^T buffer b is free once the PV of tile j-2 completed
             if (j >= 2) wait_or_flag(&pv_done[b], (uint32_t)((j - 2) >> 1) & 1u, p.d_err);
             {
+                // P of head h is stored twice: rounded to the input type in
+                // row h, and the rounding residual (rounded again) in row 8 + h,
+                // the MMA's padding rows.  The PV MMA then yields V.P_hi in
+                // column h and V.P_lo in column 8 + h of O^T, and their fp32
+                // sum carries P to about twice the input type's precision at
+                // no extra MMA (a 16-bit P alone would add up to 2^-9 |v|
+                // per weight to bf16 outputs)
                 const uint32_t pb = sb + kOffP + b * 4096 + (t >> 6) * 2048 + (t & 7) * 2;
                 const int ch = (t & 63) >> 3;
 #pragma unroll
                 for (int h = 0; h < kTG; h += 2) {
                     const uint32_t w2 = Elem<T>::pack2(pr[h], pr[h + 1]);
+                    float h0, h1;
+                    Elem<T>::unpack2(w2, h0, h1);
+                    const uint32_t r2 = Elem<T>::pack2(pr[h] - h0, pr[h + 1] - h1);
                     sts16(pb + h * 128 + ((ch ^ h) << 4), (uint16_t)(w2 & 0xffffu));
                     sts16(pb + (h + 1) * 128 + ((ch ^ (h + 1)) << 4), (uint16_t)(w2 >> 16));
+                    sts16(pb + (kTG + h) * 128 + ((ch ^ h) << 4), (uint16_t)(r2 & 0xffffu));
+                    sts16(pb + (kTG + h + 1) * 128 + ((ch ^ (h + 1)) << 4), (uint16_t)(r2 >> 16));
                 }
             }
             if (j == ntiles - 1 && key >= ntok) {
@@ -443,8 +451,13 @@ __global__ void __launch_bounds__(kThreads, 2)
         wait_or_flag(&pv_done[(ntiles - 1) & 1], (uint32_t)((ntiles - 1) >> 1) & 1u, p.d_err);
         tc_fence_after();
         float o[kTG];
-        tmem_ld8(tmem + lane_off + kColO, o);
-        tmem_wait_ld();
+        {
+            float o2[2 * kTG];
+            tmem_ld16(tmem + lane_off + kColO, o2);
+            tmem_wait_ld();
+#pragma unroll
+            for (int h = 0; h < kTG; ++h) o[h] = o2[h] + o2[kTG + h];  // V.P_hi + V.P_lo
+        }
         const int d = t;  // O^T row = dimension
         if (direct) {
 #pragma unroll

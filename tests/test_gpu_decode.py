@@ -415,3 +415,12 @@ def test_hundreds_of_partitions_merge_in_the_reduce(G, dtype):
     # short sequences that fit one partition and write their output directly
     c = wl.make_decode_case(f"many_parts_g{G}", [60000, 5, 129, 3000], 2 * G, 2, 128, 16, dtype, seed=140 + G)
     parity(c, partition_tokens=128)
+
+
+@pytest.mark.parametrize("G,Hkv", [(4, 8), (8, 16)])
+def test_large_batch_of_short_sequences(G, Hkv):
+    # 4096 sequences: tens of thousands of CTAs (units = sequences x kv heads),
+    # every sequence against the oracle
+    lens = np.random.default_rng(7).integers(1, 65, size=4096)
+    c = wl.make_decode_case(f"big_batch_g{G}", lens, G * Hkv, Hkv, 128, 16, "bf16", seed=150 + G)
+    parity(c)
