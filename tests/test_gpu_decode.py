@@ -424,3 +424,29 @@ def test_large_batch_of_short_sequences(G, Hkv):
     lens = np.random.default_rng(7).integers(1, 65, size=4096)
     c = wl.make_decode_case(f"big_batch_g{G}", lens, G * Hkv, Hkv, 128, 16, "bf16", seed=150 + G)
     parity(c)
+
+
+def _random_configs(n, seed):
+    rng = np.random.default_rng(seed)
+    out = []
+    for i in range(n):
+        D = int(rng.choice([64, 128]))
+        G = int(rng.choice([1, 2, 4, 8]))
+        Hkv = int(rng.integers(1, 5))
+        bs = int(rng.choice([8, 16, 32, 64, 128]))
+        dtype = str(rng.choice(["f16", "bf16"]))
+        B = int(rng.integers(1, 24))
+        lens = [int(x) for x in rng.integers(0, 3000, size=B)]
+        lens[int(rng.integers(0, B))] = int(rng.integers(1, 4))          # always one very short context
+        pt = int(rng.choice([0, bs, 4 * bs, 128 * ((bs + 127) // 128), 1024]))
+        out.append((i, D, G, Hkv, bs, dtype, lens, pt))
+    return out
+
+
+@pytest.mark.parametrize("i,D,G,Hkv,bs,dtype,lens,pt", _random_configs(24, 2026))
+def test_random_shapes_lengths_and_partitions(i, D, G, Hkv, bs, dtype, lens, pt):
+    # seeded random configurations over every supported head_dim, group,
+    # block size, dtype and partition length, ragged lengths including empty
+    # contexts: both decode kernels against the oracle
+    c = wl.make_decode_case(f"rand{i}", lens, G * Hkv, Hkv, D, bs, dtype, seed=200 + i)
+    parity(c, partition_tokens=pt)
