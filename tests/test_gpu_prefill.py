@@ -252,3 +252,29 @@ def test_prefill_scores_growing_along_the_keys_rescale_the_accumulator(G, dtype)
                                num_threads=8)
     out = run_prefill(case, t)
     check_attention(to_f64(out), ref, dtype, case.name)
+
+
+def _random_prefill_configs(n, seed):
+    rng = np.random.default_rng(seed)
+    out = []
+    for i in range(n):
+        P = int(rng.choice([0, int(rng.integers(1, 1500))]))
+        C = int(rng.integers(1, 300))
+        G = int(rng.choice([1, 2, 4, 8]))
+        Hkv = int(rng.integers(1, 4))
+        bs = int(rng.choice([16, 32, 64, 128]))
+        dtype = str(rng.choice(["f16", "bf16"]))
+        out.append((i, P, C, G, Hkv, bs, dtype))
+    return out
+
+
+@pytest.mark.parametrize("i,P,C,G,Hkv,bs,dtype", _random_prefill_configs(12, 2027))
+def test_prefill_random_shapes(i, P, C, G, Hkv, bs, dtype):
+    case = wl.make_prefill_case(f"pfrand{i}", P, C, G * Hkv, Hkv, 128, bs, dtype, seed=300 + i)
+    t = case.materialize(DEV)
+    kc, vc = wl.bits(t["k_cache"]), wl.bits(t["v_cache"])
+    assert oracle.reshape_and_cache(wl.bits(t["new_key"]), wl.bits(t["new_value"]), kc, vc,
+                                    case.slot_mapping, bs) == 0
+    ref = oracle.prefill_chunk(wl.bits(t["query"]), kc, vc, case.block_table, P, case.scale, dtype, num_threads=8)
+    out = run_prefill(case, t)
+    check_attention(to_f64(out), ref, dtype, case.name)
