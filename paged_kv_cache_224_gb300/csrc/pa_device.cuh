@@ -75,6 +75,14 @@ __device__ __forceinline__ uint64_t policy_evict_first() {
     return pol;
 }
 
+// L2 policy for data that other CTAs read again soon (a prompt's prefix K/V,
+// read by every row tile of its kv head): evict last.
+__device__ __forceinline__ uint64_t policy_evict_last() {
+    uint64_t pol;
+    asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol));
+    return pol;
+}
+
 // 1-D bulk copy global -> shared (TMA engine), completion signalled on `bar`
 // as transaction bytes.  dst, src 16-byte aligned; bytes a multiple of 16.
 __device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t bytes, uint64_t *bar,

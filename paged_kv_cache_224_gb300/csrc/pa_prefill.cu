@@ -8,19 +8,18 @@
 //
 // One CTA computes two tiles of 128 query rows -- 256/G chunk positions times
 // the G query heads of one kv head -- against 128-key tiles that both Q tiles
-// share (each K/V byte brought into shared memory serves 256 rows).  CTAs run
-// in clusters of two on adjacent row ranges of the same kv head, and each
-// K/V tile is fetched once for the pair: each CTA copies one 64-dim half of
-// every block of the tile and multicasts it into both CTAs' shared memory
-// (the TMA unit's cost is per copy, and with 16-row blocks the copies are
-// small).
-//   warp 0    TMA producer: for each key tile, one 2-D tensor copy per
-//             (block, 64-dim half) of K and of V, straight from the paged pool
-//             into a 128-byte-swizzled shared layout.  K and V have rings of
-//             their own (two stages each): K(j) is free once the QKs of tile
-//             j ran, a whole MMA round before V(j), so K(j+2) streams in while
-//             V(j) is still in use.  Block-table entries are read 32 at a
-//             time, a chunk ahead;
+// share (each K/V byte brought into shared memory serves 256 rows).
+//   warp 0    TMA producer: for each key tile, one 4-D tensor copy per block
+//             of K and of V, straight from the paged pool into a
+//             128-byte-swizzled shared layout in which the tile's 8-key groups
+//             sit 2 KB apart and the two 64-dim halves 1 KB apart inside each
+//             group (uniform strides across the tile's blocks, so one
+//             descriptor covers the tile, and one copy per block instead of
+//             one per (block, half): the copy engine's cost is per copy).  K
+//             and V have rings of their own (two stages each): K(j) is free
+//             once the QKs of tile j ran, a whole MMA round before V(j), so
+//             K(j+2) streams in while V(j) is still in use.  Block-table
+//             entries are read 32 at a time, a chunk ahead;
 //   warp 1    MMA issuer (one thread): per key tile j and Q tile g, first
 //             O_g += P_g(j-1) V(j-1), then S_g = Q_g K(j)^T, tcgen05.mma
 //             kind::f16 with fp32 accumulation in TMEM.  P_g is written over
@@ -56,8 +55,7 @@ constexpr int kNK = 128;                       // keys per tile
 constexpr int kStages = 2;                     // K/V tiles in flight
 constexpr int kQHalf = kM * 128;               // one 64-dim half of a Q tile: 128 rows x 128 bytes
 constexpr int kQTile = 2 * kQHalf;             // 32 KB
-constexpr int kKVHalf = kNK * 128;             // one 64-dim half of a K or V tile
-constexpr int kKVTile = 2 * kKVHalf;           // 32 KB
+constexpr int kKVTile = kNK * kD * 2;          // 32 KB: [16 key groups][2 dim halves][8 keys][128 B]
 constexpr int kOffQ = 0;
 constexpr int kOffK = kOffQ + kQT * kQTile;                // 64 KB: K ring
 constexpr int kOffV = kOffK + kStages * kKVTile;           // 128 KB: V ring
@@ -65,8 +63,6 @@ constexpr int kOffBar = kOffV + kStages * kKVTile;         // 192 KB
 constexpr int kSmemUsed = kOffBar + 256;
 constexpr int kSmemAlloc = kSmemUsed + 1024;               // room to align the base to 1 KB
 constexpr int kThreads = 64 + kQT * 128;
-constexpr int kCluster = 2;                    // CTAs sharing each K/V tile
-constexpr uint16_t kClusterMask = (1u << kCluster) - 1;
 // TMEM columns: S of each Q tile (128 fp32; P overwrites its first 64 columns
 // as 128 packed pairs), O of each Q tile (128 fp32)
 constexpr uint32_t kColS = 0, kColO = 256;
@@ -80,8 +76,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                       const __grid_constant__ CUtensorMap tmv) {
     constexpr bool kBf16 = std::is_same<T, __nv_bfloat16>::value;
     constexpr int kBlocksPerTile = kNK / BS;
-    static_assert(kNK % BS == 0 && kBlocksPerTile <= 32 && 32 % kBlocksPerTile == 0, "block_size");
-    static_assert(kCluster == 2, "the CTAs of a pair copy one 64-dim half of every block each");
+    static_assert(kNK % BS == 0 && BS % 8 == 0 && 32 % kBlocksPerTile == 0, "block_size");
     static_assert(kM % G == 0, "group");
 
     extern __shared__ unsigned char smem_raw[];
@@ -103,7 +98,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     pdl_wait();  // the kernel before this one on the stream (the chunk's cache write) has finished
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int kvh = blockIdx.y;
-    const int rank = (int)cluster_rank();
     // the sequence of this CTA: the last one whose first CTA is at or before it
     int si = 0;
     for (int i = 1; i < p.num_seqs; ++i)
@@ -113,19 +107,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int cta = (int)blockIdx.x - sq.cta_start;  // CTA index within the sequence
     const int row0 = cta * (kQT * kM);
     const int nrows = chunk_len * G;
-    // both CTAs of a cluster walk the same key tiles: up to the last key any
-    // row of the cluster sees (cta_start is a multiple of the cluster size)
-    const int cl_row_end = (cta - rank + kCluster) * (kQT * kM);
-    const int i_last = max(0, min(chunk_len - 1, (cl_row_end - 1) / G));
+    // key tiles up to the last key any row of this CTA sees
+    const int i_last = max(0, min(chunk_len - 1, (row0 + kQT * kM - 1) / G));
     const int kend = prefix_len + i_last;
     const int ntiles = kend / kNK + 1;
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < kStages; ++i) {
             mbar_init(&k_full[i], 1);
-            mbar_init(&k_empty[i], kCluster);  // released by the MMA issuer of each CTA
+            mbar_init(&k_empty[i], 1);
             mbar_init(&v_full[i], 1);
-            mbar_init(&v_empty[i], kCluster);
+            mbar_init(&v_empty[i], 1);
         }
         mbar_init(q_full, kQT * 128);
         for (int g = 0; g < kQT; ++g) {
@@ -144,14 +136,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     tc_fence_before();
     __syncthreads();
-    cluster_sync();  // the peer's copies and releases may target these barriers from here on
     tc_fence_after();
     const uint32_t tmem = *tmem_holder;
 
     if (warp == 0) {
         // ============================================================ producer
         const int32_t *table = sq.block_table;
-        const int oob_row = p.num_blocks * p.num_kv_heads * BS;  // first row past the pool: zero fill
+        const int oob = p.num_blocks * p.num_kv_heads * (BS / 8);  // first 8-row group past the pool: zero fill
+        const uint64_t pol = policy_evict_last();  // every row tile of this kv head reads the same K/V
         // Table entries come 32 at a time, one per lane, a whole chunk ahead of
         // use (a chunk covers 32 / kBlocksPerTile tiles), so the producer never
         // waits on a table load; lane b < kBlocksPerTile handles block b of a tile.
@@ -159,11 +151,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         auto chunk = [&](int c) { return c * 32 + lane < nent ? table[c * 32 + lane] : -1; };
         int ent_cur = chunk(0), ent_nxt = chunk(1);
         constexpr int kTilesPerChunk = 32 / kBlocksPerTile;
-        // row of block `lane` of tile j in the pool (zero-fill row when past kend)
-        auto tile_row = [&](int j, int blk) {
-            int y = oob_row;
+        // first 8-row group of block `lane` of tile j in the pool (zero fill when past kend)
+        auto tile_y = [&](int j, int blk) {
+            int y = oob;
             if (lane < kBlocksPerTile && j * kNK + lane * BS <= kend) {
-                if (blk >= 0 && blk < p.num_blocks) y = (blk * p.num_kv_heads + kvh) * BS;
+                if (blk >= 0 && blk < p.num_blocks) y = (blk * p.num_kv_heads + kvh) * (BS / 8);
                 else flag_error(p.d_err, PA_DEVERR_BLOCK_RANGE);
             }
             return y;
@@ -175,38 +167,44 @@ __global__ void __launch_bounds__(kThreads, 1)
                 mbar_arrive_expect_tx(&full[st], (uint32_t)kKVTile);
             }
             __syncwarp();
-            if (lane < kBlocksPerTile) {
-                // this CTA's 64-dim half of block `lane`, into both CTAs of the pair
-                const uint32_t dst = ring + st * kKVTile + rank * kKVHalf + lane * BS * 128;
-                tma_2d_mc(dst, map, rank * 64, y, &full[st], kClusterMask);
-            }
+            // block `lane`: both 64-dim halves of its BS rows, BS * 256 bytes
+            if (lane < kBlocksPerTile) tma_4d(ring + st * kKVTile + lane * (BS * 256), map, y, &full[st], pol);
         };
         // order: K(0), then K(j) before V(j-1) -- both are first needed by the
         // same MMA round, and K(j)'s slot frees up earlier
-        int y_prev = oob_row;
+        int y_prev = oob;
         for (int j = 0; j < ntiles; ++j) {
             if (j > 0 && j % kTilesPerChunk == 0) {
                 ent_cur = ent_nxt;
                 ent_nxt = chunk(j / kTilesPerChunk + 1);
             }
             const int blk = __shfl_sync(0xffffffffu, ent_cur, (j % kTilesPerChunk) * kBlocksPerTile + (lane % kBlocksPerTile));
-            const int y = tile_row(j, blk);
+            const int y = tile_y(j, blk);
             load(&tmk, k_full, k_empty, sb + kOffK, j, y);
             if (j >= 1) load(&tmv, v_full, v_empty, sb + kOffV, j - 1, y_prev);
             y_prev = y;
         }
         load(&tmv, v_full, v_empty, sb + kOffV, ntiles - 1, y_prev);
+        // every copy has normally been consumed by now; after a timeout, let
+        // the ones in flight land before the CTA can exit
+        if (lane == 0) {
+            for (int j = max(0, ntiles - kStages); j < ntiles; ++j) {
+                mbar_wait(&k_full[j % kStages], (uint32_t)(j / kStages) & 1u);
+                mbar_wait(&v_full[j % kStages], (uint32_t)(j / kStages) & 1u);
+            }
+        }
     } else if (warp == 1) {
         // ============================================================ MMA issuer
         if (lane == 0) {
             constexpr uint32_t idesc_qk = instr_desc(kBf16, false, false, kM, kNK);
             constexpr uint32_t idesc_pv = instr_desc(kBf16, false, true, kM, kD);
-            constexpr uint32_t hi = desc_hi(1024);
+            constexpr uint32_t hi_q = desc_hi(1024);   // Q: 8-row groups 1 KB apart
+            constexpr uint32_t hi_kv = desc_hi(2048);  // K, V: 8-key groups 2 KB apart
             // descriptor low words of Q tile 0 and of stage 0's K and V; the
             // rest are fixed offsets from these
             const uint32_t q_lo0 = desc_lo(sb + kOffQ, 16);
-            const uint32_t k_lo0 = desc_lo(sb + kOffK, 16);
-            const uint32_t v_lo0 = desc_lo(sb + kOffV, kKVHalf);
+            const uint32_t k_lo0 = desc_lo(sb + kOffK, 16);     // K-major: leading offset unused
+            const uint32_t v_lo0 = desc_lo(sb + kOffV, 1024);   // MN-major: second 64-dim half 1 KB on
             wait_or_flag(q_full, 0, p.d_err);
             tc_fence_after();
             for (int j = 0; j <= ntiles; ++j) {
@@ -222,11 +220,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                         const uint32_t v_lo = v_lo0 + stp * (kKVTile >> 4);
 #pragma unroll
                         for (int kk = 0; kk < kNK / 16; ++kk)
-                            mma_f16_ts(tmem + kColO + g * kD, tS + kk * 8, desc_of(v_lo + kk * (2048 >> 4), hi),
+                            mma_f16_ts(tmem + kColO + g * kD, tS + kk * 8, desc_of(v_lo + kk * (4096 >> 4), hi_kv),
                                        idesc_pv, j > 1 || kk > 0);
                         if (j == ntiles) mma_commit(&o_done[g]);
                         // release V(j-1)'s slot only if the producer will wait for it
-                        if (g == kQT - 1 && j - 1 + kStages < ntiles) mma_commit_mc(&v_empty[stp], kClusterMask);
+                        if (g == kQT - 1 && j - 1 + kStages < ntiles) mma_commit(&v_empty[stp]);
                     }
                     if (j < ntiles) {
                         if (g == 0) {
@@ -239,11 +237,11 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                         for (int kk = 0; kk < 8; ++kk) {
                             const uint32_t qo = ((kk >> 2) * kQHalf + (kk & 3) * 32) >> 4;
-                            const uint32_t ko = ((kk >> 2) * kKVHalf + (kk & 3) * 32) >> 4;
-                            mma_f16(tS, desc_of(q_lo + qo, hi), desc_of(k_lo + ko, hi), idesc_qk, kk > 0);
+                            const uint32_t ko = ((kk >> 2) * 1024 + (kk & 3) * 32) >> 4;
+                            mma_f16(tS, desc_of(q_lo + qo, hi_q), desc_of(k_lo + ko, hi_kv), idesc_qk, kk > 0);
                         }
                         mma_commit(&s_full[g]);
-                        if (g == kQT - 1 && j + kStages < ntiles) mma_commit_mc(&k_empty[st], kClusterMask);
+                        if (g == kQT - 1 && j + kStages < ntiles) mma_commit(&k_empty[st]);
                     }
                 }
             }
@@ -380,7 +378,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const uint32_t v_s = sb + kOffV + st_kv * kKVTile;
                 for (int idx = t; idx < (kNK - z0) * 16; idx += 128) {
                     const int r = z0 + (idx >> 4), h = (idx >> 3) & 1, c = idx & 7;
-                    asm volatile("st.shared.v4.u32 [%0], {%1,%1,%1,%1};" ::"r"(v_s + h * kKVHalf + r * 128 + c * 16),
+                    asm volatile("st.shared.v4.u32 [%0], {%1,%1,%1,%1};" ::"r"(
+                                     v_s + (r >> 3) * 2048 + h * 1024 + (r & 7) * 128 + c * 16),
                                  "r"(0u)
                                  : "memory");
                 }
@@ -416,7 +415,6 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     tc_fence_before();
     __syncthreads();
-    cluster_sync();  // neither CTA leaves while the other may still copy into it
     if (warp == 1) {
         tc_fence_after();
         asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols)
@@ -426,16 +424,17 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 // ---- host side -------------------------------------------------------------
 
-// The pool as a 2-D tensor [num_blocks*num_kv_heads*block_size rows][128]; a
-// box is 64 elements (128 bytes) by block_size rows, 128-byte swizzled.
+// The pool as a 4-D tensor {64 dims, 8 rows, 2 dim halves, 8-row groups}
+// with strides {2, 256, 128, 2048} bytes; a box is one block (block_size / 8
+// groups), landing as [group][half][8 rows][128 B], 128-byte swizzled.
 bool make_pool_map(CUtensorMap *map, const void *pool, const PrefillParams &p, int bs, bool bf16) {
     EncodeTiledFn fn = encode_fn();
     if (!fn) return false;
-    const cuuint64_t dims[2] = {(cuuint64_t)kD, (cuuint64_t)p.num_blocks * p.num_kv_heads * bs};
-    const cuuint64_t strides[1] = {(cuuint64_t)kD * 2};
-    const cuuint32_t box[2] = {64, (cuuint32_t)bs};
-    const cuuint32_t estr[2] = {1, 1};
-    return fn(map, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2,
+    const cuuint64_t dims[4] = {64, 8, 2, (cuuint64_t)p.num_blocks * p.num_kv_heads * (bs / 8)};
+    const cuuint64_t strides[3] = {(cuuint64_t)kD * 2, 128, (cuuint64_t)8 * kD * 2};
+    const cuuint32_t box[4] = {64, 8, 2, (cuuint32_t)(bs / 8)};
+    const cuuint32_t estr[4] = {1, 1, 1, 1};
+    return fn(map, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 4,
               const_cast<void *>(pool), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
               CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
@@ -455,16 +454,12 @@ int launch_tc_t(const PrefillParams &p, cudaStream_t stream) {
     cfg.blockDim = dim3(kThreads);
     cfg.dynamicSmemBytes = kSmemAlloc;
     cfg.stream = stream;
-    cudaLaunchAttribute attr[2];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = kCluster;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
+    cudaLaunchAttribute attr[1];
     // programmatic dependent launch: scheduled while the cache write drains
-    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[1].val.programmaticStreamSerializationAllowed = 1;
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 2;
+    cfg.numAttrs = 1;
     return cudaLaunchKernelEx(&cfg, kern, p, tmk, tmv) == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }
 
@@ -490,15 +485,14 @@ int launch_prefill(pa_dtype dt, int head_dim, int block_size, int group, const P
     // TMA row coordinates are 32-bit
     if ((long long)p_in.num_blocks * p_in.num_kv_heads * block_size >= (1LL << 31)) return PA_ERR_UNSUPPORTED;
     if (p_in.num_seqs < 1 || p_in.num_seqs > kPrefillMaxSeqs) return PA_ERR_INVALID_ARG;
-    // each sequence's CTAs: its rows (chunk positions x group) in tiles of
-    // kQT*kM, rounded up to whole clusters so no cluster spans two sequences
+    // each sequence's CTAs: its rows (chunk positions x group) in tiles of kQT*kM
     PrefillParams p = p_in;
     long long ctas = 0;
     for (int i = 0; i < p.num_seqs; ++i) {
         p.seqs[i].cta_start = (int)ctas;
         const long long rows = (long long)p.seqs[i].chunk_len * group;
         const long long tiles = (rows + kQT * kM - 1) / (kQT * kM);
-        ctas += (tiles + kCluster - 1) / kCluster * kCluster;
+        ctas += tiles;
     }
     if (ctas == 0) return PA_OK;
     if (ctas > 0x7fffffffLL) return PA_ERR_UNSUPPORTED;

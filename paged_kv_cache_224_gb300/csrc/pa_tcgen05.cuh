@@ -145,18 +145,6 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const float (&v)[16]) 
 __device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 __device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
-// 2-D tensor copy global -> shared, written to the same offset in every CTA
-// of the cluster named in cta_mask, completing bytes on the barrier at the
-// same offset in each.
-__device__ __forceinline__ void tma_2d_mc(uint32_t dst, const CUtensorMap *map, int x, int y, uint64_t *bar,
-                                          uint16_t cta_mask) {
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.multicast::cluster"
-        " [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(dst),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_addr(bar)), "h"(cta_mask)
-        : "memory");
-}
-
 // 4-D tensor copy global -> shared of the box at (0, 0, 0, y), completing
 // bytes on `bar`, with an L2 cache policy.
 __device__ __forceinline__ void tma_4d(uint32_t dst, const CUtensorMap *map, int y, uint64_t *bar, uint64_t policy) {
@@ -170,26 +158,6 @@ __device__ __forceinline__ void tma_4d(uint32_t dst, const CUtensorMap *map, int
 // Barrier `id` (1-15) over `count` threads (a multiple of 32).
 __device__ __forceinline__ void named_bar_sync(int id, int count) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
-}
-
-// Arrive (once) on the barrier at this offset in every CTA of cta_mask when
-// all MMAs issued so far by this thread have completed.
-__device__ __forceinline__ void mma_commit_mc(uint64_t *bar, uint16_t cta_mask) {
-    asm volatile(
-        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
-            smem_addr(bar)),
-        "h"(cta_mask)
-        : "memory");
-}
-
-__device__ __forceinline__ uint32_t cluster_rank() {
-    uint32_t r;
-    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-    return r;
-}
-
-__device__ __forceinline__ void cluster_sync() {
-    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 
 __device__ __forceinline__ void mbar_arrive1(uint64_t *bar) {
