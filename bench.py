@@ -466,7 +466,10 @@ def main():
                                          case.max_context_len, pt)
     max_parts = -(-case.max_context_len // part)
     pairs = torch.as_tensor(case.cow_pairs, device=dev) if case.cow_pairs.shape[0] else None
-    launches_per_step = (1 if pairs is not None else 0) + 1 + (3 if grouped else 1 + (1 if max_parts > 1 else 0))
+    cow_ws = (torch.empty(pa.pa_copy_blocks_workspace_bytes(pairs.shape[0]), dtype=torch.uint8, device=dev)
+              if pairs is not None else None)
+    # copy-on-write: clear, count and copy kernels
+    launches_per_step = (3 if pairs is not None else 0) + 1 + (3 if grouped else 1 + (1 if max_parts > 1 else 0))
 
     def decode(q, bt_, lens_):
         if grouped:
@@ -480,7 +483,7 @@ def main():
     def cow():
         # copy-on-write of shared blocks before the tails are written (idempotent across steps)
         if pairs is not None:
-            pa.pa_copy_blocks(t["k_cache"], t["v_cache"], pairs, d_err=err)
+            pa.pa_copy_blocks(t["k_cache"], t["v_cache"], pairs, d_err=err, workspace=cow_ws)
 
     def step():
         cow()

@@ -80,8 +80,10 @@ PA_API const char *pa_status_string(int status);
 
 /*
  * pa_reshape_and_cache -- write new tokens' K and V rows into their slots.
- * (Dynamic growth of a sequence: each new token lands in a slot of one of
- * its physical blocks; chunked prefill accumulates a chunk's KV the same way.)
+ * ("vLLM PagedAttention chuyen sau" (locionic.com), section "Tuong tu phan
+ * trang bo nho ao": a growing sequence gets each new token a slot in one of
+ * its physical blocks; section "Chunked Prefill", mechanism step 3: a
+ * chunk's KV accumulates in the cache the same way.)
  *
  *   key, value     [num_tokens][num_kv_heads][head_dim] dtype, contiguous
  *   k_cache,v_cache pool as above, written in place
@@ -312,22 +314,40 @@ PA_API int pa_bounded_wait_polls(void);
 PA_API int pa_selftest_bounded_wait(int max_polls, int *d_err, long long *d_cycles, void *stream);
 
 /*
- * pa_copy_blocks -- copy-on-write: for each pair (src, dst) of `pairs`
- * (int64 [num_pairs][2]), copy the whole K block and V block (all kv heads)
- * of src to dst, bit-exact.  A pair is skipped and PA_DEVERR_COPY_PAIR set
- * when an id is outside the pool, src == dst, its dst appears as another
- * pair's dst, or its dst is any pair's src -- so the result never depends on
- * the order in which pairs run.  Each pair costs an O(num_pairs) scan of the
- * list on the device.
+ * pa_copy_blocks -- copy-on-write of shared blocks ("vLLM PagedAttention
+ * chuyen sau" (locionic.com), section "Co che APC", step 3: a block that
+ * several sequences share is copied before one of them writes into it).
+ * For each pair (src, dst) of `pairs` (int64 [num_pairs][2], device), copy
+ * the whole K block and V block (all kv heads) of src to dst, bit-exact.  A
+ * pair is skipped and PA_DEVERR_COPY_PAIR set when an id is outside the
+ * pool, src == dst, its dst appears as another pair's dst, or its dst is any
+ * pair's src -- so the result never depends on the order in which pairs run.
+ *
+ *   workspace  device scratch of at least
+ *              pa_copy_blocks_workspace_bytes(num_pairs) bytes, 16-byte
+ *              aligned, owned by the caller (NULL allowed when num_pairs is
+ *              0).  The call counts, in one pass over the pairs, how often
+ *              each block id appears as a dst and as a src (a hash table in
+ *              the workspace); each pair's copy then reads its dst's counts
+ *              once, so validation costs O(num_pairs) in total.  Its content
+ *              on entry is ignored; it must not be shared with work that
+ *              overlaps the call on the device.
+ * num_pairs above PA_COPY_MAX_PAIRS returns PA_ERR_OUT_OF_RANGE; a missing
+ * or too small workspace returns PA_ERR_WORKSPACE.  Three launches (clear
+ * the table, count, copy).
  */
+#define PA_COPY_MAX_PAIRS (1 << 26)
+PA_API size_t pa_copy_blocks_workspace_bytes(int num_pairs);
 PA_API int pa_copy_blocks(void *k_cache, void *v_cache, const int64_t *pairs, int num_pairs,
                    int num_kv_heads, int head_dim, int block_size, int num_blocks,
-                   pa_dtype dtype, int *d_err, void *stream);
+                   pa_dtype dtype, void *workspace, size_t workspace_bytes, int *d_err, void *stream);
 
 /*
  * pa_prefill_chunk -- attention of one prompt chunk over its sequence's paged
- * KV, causal: row i (absolute position prefix_len + i) attends to keys
- * 0 .. prefix_len + i.  The chunk's own K/V must already be in the cache
+ * KV ("vLLM PagedAttention chuyen sau" (locionic.com), section "Chunked
+ * Prefill", mechanism: a long prompt is processed chunk by chunk, each chunk
+ * attending to the KV its sequence has accumulated so far), causal: row i
+ * (absolute position prefix_len + i) attends to keys 0 .. prefix_len + i.  The chunk's own K/V must already be in the cache
  * (pa_reshape_and_cache).  QK^T and PV run on the 5th-generation tensor cores
  * (tcgen05.mma, accumulators in TMEM) with fp32 accumulation; P is rounded
  * to dtype for the PV product;

@@ -3,7 +3,8 @@
 The product is the C-ABI library ``libpa.so`` (``include/pa.h``); ``capi``
 binds it for torch tensors.  ``workload`` draws seeded synthetic inputs.
 """
-from .capi import (PAError, lib, pa_copy_blocks, pa_decode, pa_decode_partition_tokens,  # noqa: F401
+from .capi import (PAError, lib, pa_copy_blocks, pa_copy_blocks_workspace_bytes, pa_decode,  # noqa: F401
+                   pa_decode_partition_tokens,
                    pa_decode_noalloc, pa_decode_shared_prefix, pa_decode_shared_prefix_workspace_bytes,
                    pa_decode_workspace_bytes, pa_decode_step_host, pa_decode_step_host_staging_bytes,
                    pa_mixed_step, pa_prefill_batch, pa_prefill_chunk, pa_reshape_and_cache,

@@ -22,9 +22,10 @@ LIB_PATH = os.path.join(_HERE, "libpa.so")
 
 PA_F16, PA_BF16 = 0, 1
 DEVERR = {"slot_range": 0x1, "block_range": 0x2, "context_range": 0x4, "copy_pair": 0x8,
-          "timeout": 0x10}
+          "timeout": 0x10, "prefix": 0x20}
 EXPORTED = ("pa_status_string", "pa_reshape_and_cache", "pa_decode_partition_tokens",
-            "pa_decode_workspace_bytes", "pa_decode", "pa_copy_blocks", "pa_prefill_chunk",
+            "pa_decode_workspace_bytes", "pa_decode", "pa_copy_blocks_workspace_bytes", "pa_copy_blocks",
+            "pa_prefill_chunk",
             "pa_decode_noalloc", "pa_decode_shared_prefix_workspace_bytes", "pa_decode_shared_prefix",
             "pa_bm_create", "pa_bm_destroy", "pa_bm_add_sequence", "pa_bm_fork", "pa_bm_append_token",
             "pa_bm_free_sequence", "pa_bm_block_table", "pa_bm_seq_len", "pa_bm_block_refcount",
@@ -93,7 +94,9 @@ def lib() -> ctypes.CDLL:
         L.pa_bm_block_refcount.restype = i
         L.pa_bm_stats.argtypes = [p, p]
         L.pa_bm_stats.restype = i
-        L.pa_copy_blocks.argtypes = [p, p, p, i, i, i, i, i, i, p, p]
+        L.pa_copy_blocks_workspace_bytes.argtypes = [i]
+        L.pa_copy_blocks_workspace_bytes.restype = sz
+        L.pa_copy_blocks.argtypes = [p, p, p, i, i, i, i, i, i, p, sz, p, p]
         L.pa_copy_blocks.restype = i
         L.pa_prefill_chunk.argtypes = [p, p, p, p, p, i, i, i, i, i, i, i, ctypes.c_float, i, p, p]
         L.pa_prefill_chunk.restype = i
@@ -359,15 +362,25 @@ def pa_selftest_bounded_wait(max_polls, d_err, d_cycles=None, stream=None):
     _check("pa_selftest_bounded_wait", rc)
 
 
-def pa_copy_blocks(k_cache, v_cache, pairs, d_err=None, stream=None):
-    """pairs int64 [n][2] of (src, dst) physical block ids."""
-    _dev(k_cache, v_cache, pairs, d_err)
+def pa_copy_blocks_workspace_bytes(num_pairs: int) -> int:
+    return int(lib().pa_copy_blocks_workspace_bytes(int(num_pairs)))
+
+
+def pa_copy_blocks(k_cache, v_cache, pairs, d_err=None, stream=None, workspace=None):
+    """pairs int64 [n][2] of (src, dst) physical block ids.  ``workspace``:
+    a uint8 CUDA tensor of at least ``pa_copy_blocks_workspace_bytes(n)``
+    bytes; allocated here when not given."""
+    _dev(k_cache, v_cache, pairs, d_err, workspace)
     if pairs.dtype != torch.int64:
         raise TypeError("pairs must be int64")
     NB, Hkv, bs, D = k_cache.shape
     n = pairs.shape[0] if pairs.numel() else 0
+    if workspace is None:
+        workspace = torch.empty(max(1, pa_copy_blocks_workspace_bytes(n)), dtype=torch.uint8,
+                                device=k_cache.device)
     rc = lib().pa_copy_blocks(_ptr(k_cache), _ptr(v_cache), _ptr(pairs), n, Hkv, D, bs, NB,
-                              _dt(k_cache), _ptr(d_err), _stream(k_cache, stream))
+                              _dt(k_cache), _ptr(workspace), workspace.numel() * workspace.element_size(),
+                              _ptr(d_err), _stream(k_cache, stream))
     _check("pa_copy_blocks", rc)
 
 

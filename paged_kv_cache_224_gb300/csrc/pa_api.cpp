@@ -307,18 +307,26 @@ int pa_decode_shared_prefix(void *out, const void *query, const void *k_cache, c
     return pa::launch_decode_reduce(dtype, head_dim, red, st);
 }
 
+size_t pa_copy_blocks_workspace_bytes(int num_pairs) {
+    if (num_pairs < 0 || num_pairs > PA_COPY_MAX_PAIRS) return 0;
+    return pa::copy_blocks_workspace_bytes(num_pairs);
+}
+
 int pa_copy_blocks(void *k_cache, void *v_cache, const int64_t *pairs, int num_pairs,
                    int num_kv_heads, int head_dim, int block_size, int num_blocks, pa_dtype dtype,
-                   int *d_err, void *stream) {
+                   void *workspace, size_t workspace_bytes, int *d_err, void *stream) {
     if (num_pairs < 0 || num_kv_heads <= 0 || head_dim <= 0 || block_size <= 0 || num_blocks <= 0 ||
         !good_dtype(dtype))
         return PA_ERR_INVALID_ARG;
+    if (num_pairs > PA_COPY_MAX_PAIRS) return PA_ERR_OUT_OF_RANGE;
     if (num_pairs == 0) return PA_OK;
     if (!k_cache || !v_cache || !pairs) return PA_ERR_INVALID_ARG;
     if (((long long)num_kv_heads * block_size * head_dim) % 8) return PA_ERR_UNSUPPORTED;
     if (!aligned16(k_cache) || !aligned16(v_cache)) return PA_ERR_ALIGNMENT;
+    if (!workspace || workspace_bytes < pa::copy_blocks_workspace_bytes(num_pairs)) return PA_ERR_WORKSPACE;
+    if (!aligned16(workspace)) return PA_ERR_ALIGNMENT;
     return pa::launch_copy_blocks(k_cache, v_cache, pairs, num_pairs, num_kv_heads, head_dim,
-                                  block_size, num_blocks, d_err, static_cast<cudaStream_t>(stream));
+                                  block_size, num_blocks, workspace, d_err, static_cast<cudaStream_t>(stream));
 }
 
 int pa_prefill_chunk(void *out, const void *query, const void *k_cache, const void *v_cache,
@@ -418,7 +426,7 @@ size_t round256(size_t n) { return (n + 255) / 256 * 256; }
 // Staging regions of pa_decode_step_host, in order: out, query, new keys, new
 // values, slots, copy pairs, block tables, context lengths, decode workspace.
 struct StepLayout {
-    size_t off[9];
+    size_t off[10];
     size_t total;
 };
 
@@ -426,7 +434,8 @@ bool step_layout(int num_seqs, int num_heads, int num_kv_heads, int head_dim, in
                  int max_blocks_per_seq, int max_context_len, int num_new_tokens, int num_pairs, int group_size,
                  int prefix_blocks, int partition_tokens, StepLayout *lay) {
     if (num_seqs <= 0 || num_heads <= 0 || num_kv_heads <= 0 || num_heads % num_kv_heads || head_dim <= 0 ||
-        block_size <= 0 || max_blocks_per_seq <= 0 || max_context_len < 0 || num_new_tokens < 0 || num_pairs < 0)
+        block_size <= 0 || max_blocks_per_seq <= 0 || max_context_len < 0 || num_new_tokens < 0 || num_pairs < 0 ||
+        num_pairs > PA_COPY_MAX_PAIRS)
         return false;
     const size_t qbytes = (size_t)num_seqs * num_heads * head_dim * 2;
     const size_t kvbytes = (size_t)num_new_tokens * num_kv_heads * head_dim * 2;
@@ -439,11 +448,11 @@ bool step_layout(int num_seqs, int num_heads, int num_kv_heads, int head_dim, in
         ws = pa_decode_workspace_bytes(num_seqs, num_heads, num_kv_heads, head_dim, block_size, max_context_len,
                                        partition_tokens);
     }
-    const size_t sizes[9] = {qbytes, qbytes, kvbytes, kvbytes, (size_t)num_new_tokens * 8,
-                             (size_t)num_pairs * 16, (size_t)num_seqs * max_blocks_per_seq * 4,
-                             (size_t)num_seqs * 4, ws};
+    const size_t sizes[10] = {qbytes, qbytes, kvbytes, kvbytes, (size_t)num_new_tokens * 8,
+                              (size_t)num_pairs * 16, (size_t)num_seqs * max_blocks_per_seq * 4,
+                              (size_t)num_seqs * 4, pa::copy_blocks_workspace_bytes(num_pairs), ws};
     size_t at = 0;
-    for (int i = 0; i < 9; ++i) {
+    for (int i = 0; i < 10; ++i) {
         lay->off[i] = at;
         at += round256(sizes[i]);
     }
@@ -494,8 +503,10 @@ int pa_decode_step_host(void *out_host, const void *query_host, const void *new_
     int64_t *d_pairs = reinterpret_cast<int64_t *>(base + lay.off[5]);
     int32_t *d_bt = reinterpret_cast<int32_t *>(base + lay.off[6]);
     int32_t *d_lens = reinterpret_cast<int32_t *>(base + lay.off[7]);
-    void *d_ws = base + lay.off[8];
-    const size_t ws_bytes = lay.total - lay.off[8];
+    void *d_cow_ws = base + lay.off[8];
+    const size_t cow_ws_bytes = lay.off[9] - lay.off[8];
+    void *d_ws = base + lay.off[9];
+    const size_t ws_bytes = lay.total - lay.off[9];
     const size_t qbytes = (size_t)num_seqs * num_heads * head_dim * 2;
     const size_t kvbytes = (size_t)num_new_tokens * num_kv_heads * head_dim * 2;
     auto h2d = [&](void *dst, const void *src, size_t n) {
@@ -508,7 +519,7 @@ int pa_decode_step_host(void *out_host, const void *query_host, const void *new_
         !h2d(d_lens, context_lens_host, (size_t)num_seqs * 4))
         return PA_ERR_CUDA;
     int rc = pa_copy_blocks(k_cache, v_cache, d_pairs, num_pairs, num_kv_heads, head_dim, block_size, num_blocks,
-                            dtype, d_err, stream);
+                            dtype, d_cow_ws, cow_ws_bytes, d_err, stream);
     if (rc != PA_OK) return rc;
     rc = pa_reshape_and_cache(d_k, d_v, k_cache, v_cache, d_slots, num_new_tokens, num_kv_heads, head_dim,
                               block_size, num_blocks, dtype, d_err, stream);

@@ -111,9 +111,10 @@ int launch_decode_reduce(pa_dtype dt, int head_dim, const DecodeParams &p, cudaS
 int launch_reshape_and_cache(const void *key, const void *value, void *k_cache, void *v_cache,
                              const int64_t *slots, int num_tokens, int num_kv_heads, int head_dim,
                              int block_size, int num_blocks, int *d_err, cudaStream_t stream);
+size_t copy_blocks_workspace_bytes(int num_pairs);
 int launch_copy_blocks(void *k_cache, void *v_cache, const int64_t *pairs, int num_pairs,
-                       int num_kv_heads, int head_dim, int block_size, int num_blocks, int *d_err,
-                       cudaStream_t stream);
+                       int num_kv_heads, int head_dim, int block_size, int num_blocks, void *workspace,
+                       int *d_err, cudaStream_t stream);
 int launch_prefill(pa_dtype dt, int head_dim, int block_size, int group, const PrefillParams &p,
                    cudaStream_t stream);
 

@@ -75,6 +75,24 @@ def call_decode(lib, **kw):
                          a["scale"], a["pt"], a["dt"], p(a["ws"]), a["wsb"], None, None)
 
 
+def test_copy_blocks_workspace_is_linear_in_the_pairs(lib):
+    # a hash table of 16-byte entries, a power of two >= 4 per pair (at least 64)
+    assert lib.pa_copy_blocks_workspace_bytes(0) == 0
+    assert lib.pa_copy_blocks_workspace_bytes(1) == 64 * 16
+    assert lib.pa_copy_blocks_workspace_bytes(224) == 1024 * 16
+    assert lib.pa_copy_blocks_workspace_bytes(4096) == 16384 * 16
+    assert lib.pa_copy_blocks_workspace_bytes(-1) == 0
+    assert lib.pa_copy_blocks_workspace_bytes((1 << 26) + 1) == 0
+
+
+def test_python_error_bits_match_the_header(lib):
+    from paged_kv_cache_224_gb300 import capi
+    text = open(os.path.join(ROOT, "include", "pa.h")).read()
+    bits = {m.group(1).lower(): int(m.group(2), 16)
+            for m in re.finditer(r"#define\s+PA_DEVERR_(\w+)\s+0x([0-9a-fA-F]+)", text)}
+    assert bits and bits == capi.DEVERR
+
+
 def test_decode_rejects_bad_arguments_on_host(lib):
     # These return before any CUDA call, so no device is touched.
     assert call_decode(lib, out=0) == -1                  # null pointer
@@ -97,8 +115,13 @@ def test_cache_calls_reject_bad_arguments_on_host(lib):
     assert lib.pa_reshape_and_cache(buf, buf, buf, buf, None, 4, 2, 128, 16, 64, 1, None, None) == -1
     assert lib.pa_reshape_and_cache(buf, buf, buf, buf, buf, 4, 2, 12, 16, 64, 1, None, None) == -2
     assert lib.pa_reshape_and_cache(buf, buf, buf, buf, buf, 0, 2, 128, 16, 64, 1, None, None) == 0
-    assert lib.pa_copy_blocks(buf, None, buf, 3, 2, 128, 16, 64, 1, None, None) == -1
-    assert lib.pa_copy_blocks(buf, buf, buf, 0, 2, 128, 16, 64, 1, None, None) == 0
+    ws = lib.pa_copy_blocks_workspace_bytes(3)
+    assert lib.pa_copy_blocks(buf, None, buf, 3, 2, 128, 16, 64, 1, buf, ws, None, None) == -1
+    assert lib.pa_copy_blocks(buf, buf, buf, 0, 2, 128, 16, 64, 1, None, 0, None, None) == 0
+    assert lib.pa_copy_blocks(buf, buf, buf, 3, 2, 128, 16, 64, 1, None, 0, None, None) == -5   # no workspace
+    assert lib.pa_copy_blocks(buf, buf, buf, 3, 2, 128, 16, 64, 1, buf, ws - 1, None, None) == -5
+    assert lib.pa_copy_blocks(buf, buf, buf, 3, 2, 128, 16, 64, 1, p((1 << 20) + 8), ws, None, None) == -6
+    assert lib.pa_copy_blocks(buf, buf, buf, (1 << 26) + 1, 2, 128, 16, 64, 1, buf, 1 << 40, None, None) == -3
     assert lib.pa_prefill_chunk(buf, buf, buf, buf, buf, 8, 4, 7, 2, 128, 16, 64, 0.1, 1, None, None) == -1
 
 

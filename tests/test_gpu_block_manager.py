@@ -3,17 +3,22 @@
 Prompts with common prefixes (prefix-cache hits), forked samples (shared
 blocks, copy-on-write on their first decode token) and per-step growth: each
 step the manager's copy pairs go to pa_copy_blocks, its slots to
-pa_reshape_and_cache, its tables to pa_decode.  Every token's K/V is a
-function of its whole token prefix, so every sequence's attention can be
-recomputed from its logical token list alone, with no pool: the GPU output
-must match that within the attention tolerance, and the GPU pool must hold
-each sequence's K/V at the positions its table names, bit for bit.
+pa_reshape_and_cache, its tables to pa_decode.  The same copy pairs and
+slots are replayed on the CPU oracle's own pool (oracle.copy_blocks,
+oracle.reshape_and_cache), so the oracle's decode over the manager's tables
+is the checker: the GPU output must match it within the attention tolerance,
+and the GPU pool must equal the oracle's pool bit for bit.  Every token's K/V
+is also a function of its whole token prefix, so each sequence's attention is
+recomputed a second way from its logical token list alone, with no pool, and
+the GPU pool must hold each sequence's K/V at the positions its table names.
 """
 import numpy as np
 import pytest
 import torch
 
+import oracle
 import paged_kv_cache_224_gb300 as pa
+from paged_kv_cache_224_gb300 import workload as wl
 from tests.helpers import check_attention, to_f64
 
 pytestmark = pytest.mark.gpu
@@ -54,6 +59,7 @@ def test_block_manager_drives_the_kernels():
     bm = pa.BlockManager(nb, BS, prefix_cache=True)
     kc = torch.zeros((nb, HKV, BS, D), dtype=torch.float16, device=DEV)
     vc = torch.zeros_like(kc)
+    ko, vo = wl.bits(kc), wl.bits(vc)  # the oracle's pool, updated by the oracle's own cache calls
     err = torch.zeros(1, dtype=torch.int32, device=DEV)
     tokens = {}
 
@@ -63,9 +69,10 @@ def test_block_manager_drives_the_kernels():
             return
         k = np.stack([kv_row(tokens[s][:i + 1], 1) for s, i, _ in seq_slots])
         v = np.stack([kv_row(tokens[s][:i + 1], 2) for s, i, _ in seq_slots])
-        slots = torch.as_tensor([sl for _, _, sl in seq_slots], dtype=torch.int64, device=DEV)
-        pa.pa_reshape_and_cache(torch.as_tensor(k, device=DEV), torch.as_tensor(v, device=DEV), kc, vc, slots,
-                                d_err=err)
+        sl = np.array([sl for _, _, sl in seq_slots], np.int64)
+        pa.pa_reshape_and_cache(torch.as_tensor(k, device=DEV), torch.as_tensor(v, device=DEV), kc, vc,
+                                torch.as_tensor(sl, device=DEV), d_err=err)
+        assert oracle.reshape_and_cache(k.view(np.uint16), v.view(np.uint16), ko, vo, sl, BS) == 0
 
     p0 = list(rng.integers(0, 1000, size=100))
     prompts = {0: p0, 1: p0[:64] + list(rng.integers(0, 1000, size=16)), 2: list(rng.integers(0, 1000, size=37))}
@@ -97,20 +104,26 @@ def test_block_manager_drives_the_kernels():
             assert len(pairs) == 3  # the samples' first tokens land in copies of the shared partial block
         if pairs:
             pa.pa_copy_blocks(kc, vc, torch.as_tensor(pairs, dtype=torch.int64, device=DEV), d_err=err)
+            assert oracle.copy_blocks(ko, vo, np.array(pairs, np.int64)) == 0
         write(batch)
         if step in (0, 7, 19):
             seqs = sorted(tokens)
             lens = [len(tokens[s]) for s in seqs]
-            bt = torch.as_tensor(bm.tables(seqs), device=DEV)
+            tables = bm.tables(seqs)
+            bt = torch.as_tensor(tables, device=DEV)
             q = torch.as_tensor(rng.standard_normal((len(seqs), HKV * G, D)).astype(np.float16), device=DEV)
             out = torch.full_like(q, float("nan"))
             pa.pa_decode(out, q, kc, vc, bt, torch.as_tensor(lens, dtype=torch.int32, device=DEV), scale,
                          max(lens), d_err=err)
             torch.cuda.synchronize()
             assert int(err.item()) == 0
+            assert np.array_equal(wl.bits(kc), ko) and np.array_equal(wl.bits(vc), vo)
+            ref = oracle.decode(wl.bits(q), ko, vo, np.ascontiguousarray(tables, np.int32),
+                                np.array(lens, np.int32), scale, "f16", num_threads=8)
+            check_attention(to_f64(out), ref, "f16", f"step {step} vs oracle")
             qh = q.cpu().numpy()
-            ref = np.stack([logical_attention(tokens[s], qh[i], scale) for i, s in enumerate(seqs)])
-            check_attention(to_f64(out), ref, "f16", f"step {step}")
+            logical = np.stack([logical_attention(tokens[s], qh[i], scale) for i, s in enumerate(seqs)])
+            check_attention(to_f64(out), logical, "f16", f"step {step} vs logical attention")
     # the pool holds every sequence's K/V where its table says, bit for bit
     kh, vh = kc.cpu().numpy(), vc.cpu().numpy()
     for s, toks in tokens.items():

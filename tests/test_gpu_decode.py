@@ -183,6 +183,42 @@ def test_copy_blocks_bit_exact_and_conflicts_flagged():
     assert np.array_equal(k0, wl.bits(kc)) and np.array_equal(v0, wl.bits(vc))
 
 
+def test_copy_blocks_many_pairs_with_planted_conflicts():
+    # 4096 pairs over a 10000-block pool: most valid, with planted duplicate
+    # dsts, dsts that are other pairs' srcs, src == dst and ids outside the pool
+    import oracle
+    NB, Hkv, bs, D = 10000, 4, 16, 128
+    rng = np.random.default_rng(4096)
+    perm = rng.permutation(NB)
+    n = 4096
+    pairs = np.stack([perm[:n], perm[n:2 * n]], axis=1).astype(np.int64)
+    k = 64
+    pairs[rng.choice(n, k, replace=False), 1] = pairs[rng.choice(n, k, replace=False), 1]   # duplicate dsts
+    idx = rng.choice(n, k, replace=False)
+    pairs[idx, 1] = pairs[rng.choice(n, k, replace=False), 0]                                 # dst = some src
+    idx = rng.choice(n, 16, replace=False)
+    pairs[idx, 1] = pairs[idx, 0]                                                              # src == dst
+    pairs[rng.choice(n, 8, replace=False), 0] = NB + 5                                         # src outside
+    pairs[rng.choice(n, 8, replace=False), 1] = -3                                             # dst outside
+    g = torch.Generator(device=DEV).manual_seed(2)
+    kc = torch.randn((NB, Hkv, bs, D), generator=g, device=DEV, dtype=torch.float16)
+    vc = torch.randn((NB, Hkv, bs, D), generator=g, device=DEV, dtype=torch.float16)
+    k0, v0 = wl.bits(kc), wl.bits(vc)
+    bad = oracle.copy_blocks(k0, v0, pairs)
+    assert 100 < bad < n // 4
+    err = torch.zeros(1, dtype=torch.int32, device=DEV)
+    ws = torch.empty(pa.pa_copy_blocks_workspace_bytes(n), dtype=torch.uint8, device=DEV)
+    ws.fill_(0xAB)  # the workspace's content on entry must not matter
+    pa.pa_copy_blocks(kc, vc, torch.as_tensor(pairs, device=DEV), d_err=err, workspace=ws)
+    torch.cuda.synchronize()
+    assert int(err.item()) == pa.capi.DEVERR["copy_pair"]
+    assert np.array_equal(k0, wl.bits(kc)) and np.array_equal(v0, wl.bits(vc))
+    # the same call again (the table is rebuilt, the copies are idempotent)
+    pa.pa_copy_blocks(kc, vc, torch.as_tensor(pairs, device=DEV), d_err=err, workspace=ws)
+    torch.cuda.synchronize()
+    assert np.array_equal(k0, wl.bits(kc)) and np.array_equal(v0, wl.bits(vc))
+
+
 def test_copy_on_write_isolates_the_writer_on_gpu():
     c = wl.make_shared_prefix_case("cow", num_prompts=1, samples=4, prefix_len=40, max_tail=0,
                                    num_heads=8, head_dim=128, block_size=16, dtype="bf16", seed=12)

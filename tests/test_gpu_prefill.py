@@ -3,11 +3,15 @@
 A chunk of C query rows at positions P..P+C-1 attends causally over the
 paged prefix plus itself (page "vLLM PagedAttention chuyen sau", section
 "Chunked Prefill").  Checked: small ragged cases against the oracle in full,
-the full 8192-token-prefix / 512-token-chunk workload on sampled rows (the
-oracle's prefill row i equals its decode at context P+i+1, a pinned
-identity), and the pages' "KV accumulates chunk by chunk" invariant: writing
-a prompt's K/V chunk by chunk leaves the cache bit-identical to one write.
+the full 8192-token-prefix / 512-token-chunk workload on every row, a whole
+prompt prefilled chunk after chunk (each chunk's K/V written, then its
+attention over everything written so far) against one oracle prefill of the
+whole prompt, and the pages' "KV accumulates chunk by chunk" invariant:
+writing a prompt's K/V chunk by chunk leaves the cache bit-identical to one
+write.
 """
+import os
+
 import numpy as np
 import pytest
 import torch
@@ -65,7 +69,7 @@ def test_prefill_chunk_matches_oracle(P, C, G, Hkv, bs, dtype):
     check_attention(to_f64(out), ref, dtype, case.name)
 
 
-def test_prefill_full_size_sampled_rows():
+def test_prefill_full_size_every_row():
     case = wl.chunked_prefill_case()
     assert (case.prefix_len, case.chunk_len, case.num_heads, case.num_kv_heads) == (8192, 512, 64, 8)
     t = case.materialize(DEV)
@@ -80,11 +84,45 @@ def test_prefill_full_size_sampled_rows():
                                     case.block_size) == 0
     q = wl.bits(t["query"])
     out = run_prefill(case, t)
-    rows = [0, 1, 63, 64, 255, 300, 511]
-    for i in rows:
-        L = np.array([case.prefix_len + i + 1], np.int32)
-        ref = oracle.decode(q[i:i + 1], kc, vc, compact[None, :], L, case.scale, case.dtype, num_threads=8)
-        check_attention(to_f64(out[i:i + 1]), ref, case.dtype, f"row {i}")
+    ref = oracle.prefill_chunk(q, kc, vc, compact, case.prefix_len, case.scale, case.dtype,
+                               num_threads=os.cpu_count() or 8)
+    check_attention(to_f64(out), ref, case.dtype, case.name)
+
+
+@pytest.mark.parametrize("chunks,bs", [([512, 512, 512, 512], 16), ([700, 13, 1335], 16),
+                                       ([512, 512, 512, 512], 32), ([1, 300, 1747], 32)])
+def test_prompt_prefilled_chunk_after_chunk(chunks, bs):
+    # one 2048-token prompt, 64/8 heads, bf16: for each chunk, write its K/V
+    # into the paged cache, then attend over the prefix written so far plus
+    # the chunk.  Every row of every chunk must match one oracle prefill of the
+    # whole prompt over the final cache, and the final cache must equal the
+    # oracle's, bit for bit.
+    total = sum(chunks)
+    case = wl.make_prefill_case(f"prompt{len(chunks)}_{bs}", 0, total, 64, 8, 128, bs, "bf16", seed=2048 + bs)
+    t = case.materialize(DEV)
+    kc0, vc0 = wl.bits(t["k_cache"]), wl.bits(t["v_cache"])
+    assert oracle.reshape_and_cache(wl.bits(t["new_key"]), wl.bits(t["new_value"]), kc0, vc0,
+                                    case.slot_mapping, bs) == 0
+    ref = oracle.prefill_chunk(wl.bits(t["query"]), kc0, vc0, case.block_table, 0, case.scale, "bf16",
+                               num_threads=os.cpu_count() or 8)
+    slots = torch.as_tensor(case.slot_mapping, device=DEV)
+    bt = torch.as_tensor(case.block_table, device=DEV)
+    err = torch.zeros(1, dtype=torch.int32, device=DEV)
+    out = torch.full_like(t["query"], float("nan"))
+    a = 0
+    for c in chunks:
+        b = a + c
+        pa.pa_reshape_and_cache(t["new_key"][a:b].contiguous(), t["new_value"][a:b].contiguous(), t["k_cache"],
+                                t["v_cache"], slots[a:b].contiguous(), d_err=err)
+        part = torch.full_like(t["query"][a:b], float("nan"))
+        pa.pa_prefill_chunk(part, t["query"][a:b].contiguous(), t["k_cache"], t["v_cache"], bt, a, case.scale,
+                            d_err=err)
+        out[a:b] = part
+        a = b
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0, f"device error flags {int(err.item()):#x}"
+    assert np.array_equal(wl.bits(t["k_cache"]), kc0) and np.array_equal(wl.bits(t["v_cache"]), vc0)
+    check_attention(to_f64(out), ref, "bf16", case.name)
 
 
 def test_prefill_row_equals_gpu_decode_at_that_position():
