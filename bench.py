@@ -243,14 +243,17 @@ def run_prefill_bench(args, world, rank, local, dev, stream):
     bt = torch.as_tensor(case.block_tables if batch else case.block_table, device=dev)
     out = torch.empty_like(t["query"])
     err = torch.zeros(1, dtype=torch.int32, device=dev)
+    # stream-K over one CTA per SM (partials in the workspace), or one CTA per unit
+    stream_k = args.prefill_schedule == "stream_k"
+    ws = pa.prefill_workspace(t["query"], case.num_kv_heads, len(case.chunk_lens) if batch else 1) if stream_k else None
 
     def prefill():
         if batch:
             pa.pa_prefill_batch(out, t["query"], t["k_cache"], t["v_cache"], bt, case.prefix_lens, case.chunk_lens,
-                                case.scale, d_err=err)
+                                case.scale, d_err=err, workspace=ws)
         else:
             pa.pa_prefill_chunk(out, t["query"], t["k_cache"], t["v_cache"], bt, case.prefix_len, case.scale,
-                                d_err=err)
+                                d_err=err, workspace=ws)
 
     def step():
         pa.pa_reshape_and_cache(t["new_key"], t["new_value"], t["k_cache"], t["v_cache"], slots, d_err=err)
@@ -299,6 +302,8 @@ def run_prefill_bench(args, world, rank, local, dev, stream):
                            "head_dim": case.head_dim, "block_size": case.block_size,
                            "step": "pa_reshape_and_cache (chunk K/V) + "
                                    + ("pa_prefill_batch (one launch)" if batch else "pa_prefill_chunk"),
+                           "schedule": ("stream-K: one CTA per SM over equal shares of the key tiles, "
+                                        "log-sum-exp merge of split units" if stream_k else "one CTA per unit"),
                            "l2": "each kv head's KV is reused from L2 by its row tiles"},
                 "roofline": {"bound": "tensor", "achieved": round(achieved, 2), "peak": peak,
                              "unit": "TFLOP/s", "frac": round(achieved / peak, 4),
@@ -401,6 +406,8 @@ def main():
     ap.add_argument("--workload", default="llama_gqa", choices=["tiny", "llama_gqa", "opt13b_mha", "long_context", "long_context_bs32",
                              "shared_prefix", "shared_prefix_grouped", "chunked_prefill", "prefill_batch", "mixed"])
     ap.add_argument("--partition-tokens", type=int, default=0)
+    ap.add_argument("--prefill-schedule", default="stream_k", choices=["stream_k", "per_unit"],
+                    help="prefill workloads: with a workspace (stream-K) or without (one CTA per unit)")
     ap.add_argument("--e2e-steps", type=int, default=50)
     ap.add_argument("--cpu-seqs", type=int, default=64, help="sequences in the CPU-baseline sample")
     ap.add_argument("--ref-seqs", type=int, default=2, help="sequences per reference-arm step")

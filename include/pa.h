@@ -359,11 +359,29 @@ PA_API int pa_copy_blocks(void *k_cache, void *v_cache, const int64_t *pairs, in
  * scale must be finite and > 0.
  * Supported: head_dim 128, block_size in {16, 32, 64, 128}, group size in {1,2,4,8},
  * dtype f16 or bf16.
+ *
+ *   workspace  NULL, or device scratch of at least
+ *              pa_prefill_workspace_bytes(1, chunk_len, ...) bytes, 256-byte
+ *              aligned, owned by the caller, ZERO-FILLED before its first use.
+ *              The work is cut into units of 256 query rows (chunk positions
+ *              x the heads of one kv head).  With a workspace the kernel runs
+ *              one CTA per SM, each over an equal share of the units' key
+ *              tiles; a unit shared by several CTAs is finished by merging
+ *              their log-sum-exp partials, which live in the workspace with a
+ *              counter per unit.  Every call that completes leaves the
+ *              counters at zero again, so no call needs to clear anything;
+ *              after a call that set PA_DEVERR_TIMEOUT, zero-fill the
+ *              workspace again.  It must not be shared with work that overlaps
+ *              the call on the device.  Without a workspace each CTA computes
+ *              one whole unit: the same result up to rounding, slower when the
+ *              units do not fill the GPU.  A non-NULL workspace that is too
+ *              small returns PA_ERR_WORKSPACE; one not 256-byte aligned,
+ *              PA_ERR_ALIGNMENT.
  */
 PA_API int pa_prefill_chunk(void *out, const void *query, const void *k_cache, const void *v_cache,
                      const int32_t *block_table, int prefix_len, int chunk_len, int num_heads,
                      int num_kv_heads, int head_dim, int block_size, int num_blocks, float scale,
-                     pa_dtype dtype, int *d_err, void *stream);
+                     pa_dtype dtype, void *workspace, size_t workspace_bytes, int *d_err, void *stream);
 
 /*
  * pa_prefill_batch -- pa_prefill_chunk for several sequences in one launch
@@ -379,14 +397,25 @@ PA_API int pa_prefill_chunk(void *out, const void *query, const void *k_cache, c
  *                 metadata the caller knows when it builds the batch); a
  *                 chunk length of 0 skips the sequence; prefix + chunk must
  *                 fit in max_blocks_per_seq * block_size
- * Same numerics, shapes and errors as pa_prefill_chunk; one launch per 64
- * sequences with a non-empty chunk.
+ * Same numerics, shapes, workspace and errors as pa_prefill_chunk; one
+ * launch per 64 sequences with a non-empty chunk.  Without a workspace a
+ * sequence's rows are bit-identical to a pa_prefill_chunk call on it alone
+ * without one (every unit is computed whole, in the same order); with one,
+ * where the key tiles are cut depends on the whole batch.
  */
 PA_API int pa_prefill_batch(void *out, const void *query, const void *k_cache, const void *v_cache,
                             const int32_t *block_tables, int max_blocks_per_seq, const int *prefix_lens,
                             const int *chunk_lens, int num_seqs, int num_heads, int num_kv_heads,
                             int head_dim, int block_size, int num_blocks, float scale, pa_dtype dtype,
-                            int *d_err, void *stream);
+                            void *workspace, size_t workspace_bytes, int *d_err, void *stream);
+
+/*
+ * pa_prefill_workspace_bytes -- workspace for pa_prefill_chunk (num_seqs 1)
+ * or pa_prefill_batch: enough for any num_seqs chunks whose lengths add up
+ * to at most total_chunk_len, on the current device.  0 for invalid arguments.
+ */
+PA_API size_t pa_prefill_workspace_bytes(int num_seqs, int total_chunk_len, int num_heads, int num_kv_heads,
+                                         int head_dim);
 
 /*
  * Block manager -- host bookkeeping of the paged pool: which physical blocks

@@ -25,7 +25,7 @@ DEVERR = {"slot_range": 0x1, "block_range": 0x2, "context_range": 0x4, "copy_pai
           "timeout": 0x10, "prefix": 0x20}
 EXPORTED = ("pa_status_string", "pa_reshape_and_cache", "pa_decode_partition_tokens",
             "pa_decode_workspace_bytes", "pa_decode", "pa_copy_blocks_workspace_bytes", "pa_copy_blocks",
-            "pa_prefill_chunk",
+            "pa_prefill_chunk", "pa_prefill_workspace_bytes",
             "pa_decode_noalloc", "pa_decode_shared_prefix_workspace_bytes", "pa_decode_shared_prefix",
             "pa_bm_create", "pa_bm_destroy", "pa_bm_add_sequence", "pa_bm_fork", "pa_bm_append_token",
             "pa_bm_free_sequence", "pa_bm_block_table", "pa_bm_seq_len", "pa_bm_block_refcount",
@@ -98,10 +98,12 @@ def lib() -> ctypes.CDLL:
         L.pa_copy_blocks_workspace_bytes.restype = sz
         L.pa_copy_blocks.argtypes = [p, p, p, i, i, i, i, i, i, p, sz, p, p]
         L.pa_copy_blocks.restype = i
-        L.pa_prefill_chunk.argtypes = [p, p, p, p, p, i, i, i, i, i, i, i, ctypes.c_float, i, p, p]
+        L.pa_prefill_chunk.argtypes = [p, p, p, p, p, i, i, i, i, i, i, i, ctypes.c_float, i, p, sz, p, p]
         L.pa_prefill_chunk.restype = i
-        L.pa_prefill_batch.argtypes = [p, p, p, p, p, i, p, p, i, i, i, i, i, i, ctypes.c_float, i, p, p]
+        L.pa_prefill_batch.argtypes = [p, p, p, p, p, i, p, p, i, i, i, i, i, i, ctypes.c_float, i, p, sz, p, p]
         L.pa_prefill_batch.restype = i
+        L.pa_prefill_workspace_bytes.argtypes = [i, i, i, i, i]
+        L.pa_prefill_workspace_bytes.restype = sz
         L.pa_decode_step_host_staging_bytes.argtypes = [i] * 12
         L.pa_decode_step_host_staging_bytes.restype = sz
         L.pa_decode_step_host.argtypes = [p, p, p, p, p, i, p, i, p, i, p, i, i, i, i, i, i, i, i, p, p, i,
@@ -384,10 +386,30 @@ def pa_copy_blocks(k_cache, v_cache, pairs, d_err=None, stream=None, workspace=N
     _check("pa_copy_blocks", rc)
 
 
+def pa_prefill_workspace_bytes(num_seqs, total_chunk_len, num_heads, num_kv_heads, head_dim) -> int:
+    return int(lib().pa_prefill_workspace_bytes(int(num_seqs), int(total_chunk_len), int(num_heads),
+                                                int(num_kv_heads), int(head_dim)))
+
+
+def prefill_workspace(query, num_kv_heads, num_seqs=1):
+    """A zero-filled uint8 CUDA workspace big enough for prefill of ``query``'s
+    rows in ``num_seqs`` chunks (zero-filled once; the calls keep it usable)."""
+    R, Hq, D = query.shape
+    n = pa_prefill_workspace_bytes(num_seqs, R, Hq, num_kv_heads, D)
+    return torch.zeros(max(n, 1), dtype=torch.uint8, device=query.device)
+
+
+def _ws(workspace):
+    if workspace is None:
+        return ctypes.c_void_p(0), 0
+    return _ptr(workspace), workspace.numel() * workspace.element_size()
+
+
 def pa_prefill_chunk(out, query, k_cache, v_cache, block_table, prefix_len, scale, d_err=None,
-                     stream=None):
-    """out/query [C][Hq][D]; block_table int32 [>= ceil((P+C)/bs)]."""
-    _dev(out, query, k_cache, v_cache, block_table, d_err)
+                     stream=None, workspace=None):
+    """out/query [C][Hq][D]; block_table int32 [>= ceil((P+C)/bs)].  ``workspace``:
+    None (one CTA per unit) or a uint8 CUDA tensor from ``prefill_workspace``."""
+    _dev(out, query, k_cache, v_cache, block_table, d_err, workspace)
     if block_table.dtype != torch.int32:
         raise TypeError("block_table must be int32")
     NB, Hkv, bs, D = k_cache.shape
@@ -396,17 +418,19 @@ def pa_prefill_chunk(out, query, k_cache, v_cache, block_table, prefix_len, scal
         raise ValueError("shape mismatch")
     if block_table.shape[0] * bs < prefix_len + C:
         raise ValueError("block table too short for prefix + chunk")
+    wp, wb = _ws(workspace)
     rc = lib().pa_prefill_chunk(_ptr(out), _ptr(query), _ptr(k_cache), _ptr(v_cache),
                                 _ptr(block_table), int(prefix_len), C, Hq, Hkv, D, bs, NB,
-                                float(scale), _dt(query), _ptr(d_err), _stream(query, stream))
+                                float(scale), _dt(query), wp, wb, _ptr(d_err), _stream(query, stream))
     _check("pa_prefill_chunk", rc)
 
 
 def pa_prefill_batch(out, query, k_cache, v_cache, block_tables, prefix_lens, chunk_lens, scale,
-                     d_err=None, stream=None):
+                     d_err=None, stream=None, workspace=None):
     """Several sequences' chunks in one launch.  out/query [sum(chunk_lens)][Hq][D];
-    block_tables int32 [n][MB] on the device; prefix_lens, chunk_lens: n host ints."""
-    _dev(out, query, k_cache, v_cache, block_tables, d_err)
+    block_tables int32 [n][MB] on the device; prefix_lens, chunk_lens: n host ints;
+    ``workspace`` as for ``pa_prefill_chunk`` (``prefill_workspace(query, Hkv, n)``)."""
+    _dev(out, query, k_cache, v_cache, block_tables, d_err, workspace)
     if block_tables.dtype != torch.int32:
         raise TypeError("block_tables must be int32")
     NB, Hkv, bs, D = k_cache.shape
@@ -416,7 +440,8 @@ def pa_prefill_batch(out, query, k_cache, v_cache, block_tables, prefix_lens, ch
     n = int(cl.size)
     if Dq != D or out.shape != query.shape or pl.size != n or block_tables.shape[0] != n or int(cl.sum()) != R:
         raise ValueError("shape mismatch")
+    wp, wb = _ws(workspace)
     rc = lib().pa_prefill_batch(_ptr(out), _ptr(query), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables),
                                 block_tables.shape[1], pl.ctypes.data, cl.ctypes.data, n, Hq, Hkv, D, bs, NB,
-                                float(scale), _dt(query), _ptr(d_err), _stream(query, stream))
+                                float(scale), _dt(query), wp, wb, _ptr(d_err), _stream(query, stream))
     _check("pa_prefill_batch", rc)

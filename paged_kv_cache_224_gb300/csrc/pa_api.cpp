@@ -329,10 +329,19 @@ int pa_copy_blocks(void *k_cache, void *v_cache, const int64_t *pairs, int num_p
                                   block_size, num_blocks, workspace, d_err, static_cast<cudaStream_t>(stream));
 }
 
+size_t pa_prefill_workspace_bytes(int num_seqs, int total_chunk_len, int num_heads, int num_kv_heads,
+                                  int head_dim) {
+    if (num_seqs <= 0 || total_chunk_len < 0 || num_heads <= 0 || num_kv_heads <= 0 || num_heads % num_kv_heads ||
+        head_dim <= 0)
+        return 0;
+    return pa::prefill_workspace_bytes(num_seqs < pa::kPrefillMaxSeqs ? num_seqs : pa::kPrefillMaxSeqs,
+                                       total_chunk_len, num_heads / num_kv_heads, num_kv_heads);
+}
+
 int pa_prefill_chunk(void *out, const void *query, const void *k_cache, const void *v_cache,
                      const int32_t *block_table, int prefix_len, int chunk_len, int num_heads,
                      int num_kv_heads, int head_dim, int block_size, int num_blocks, float scale,
-                     pa_dtype dtype, int *d_err, void *stream) {
+                     pa_dtype dtype, void *workspace, size_t workspace_bytes, int *d_err, void *stream) {
     if (prefix_len < 0 || chunk_len < 0 || num_heads <= 0 || num_kv_heads <= 0 || head_dim <= 0 ||
         block_size <= 0 || num_blocks <= 0 || !good_dtype(dtype))
         return PA_ERR_INVALID_ARG;
@@ -353,18 +362,20 @@ int pa_prefill_chunk(void *out, const void *query, const void *k_cache, const vo
     p.num_blocks = num_blocks;
     p.scale_log2 = scale * 1.4426950408889634f;
     p.num_seqs = 1;
+    p.query_rows = chunk_len;
     p.seqs[0].block_table = block_table;
     p.seqs[0].prefix_len = prefix_len;
     p.seqs[0].chunk_len = chunk_len;
     p.seqs[0].row_start = 0;
-    return pa::launch_prefill(dtype, head_dim, block_size, num_heads / num_kv_heads, p,
+    return pa::launch_prefill(dtype, head_dim, block_size, num_heads / num_kv_heads, p, workspace, workspace_bytes,
                               static_cast<cudaStream_t>(stream));
 }
 
 int pa_prefill_batch(void *out, const void *query, const void *k_cache, const void *v_cache,
                      const int32_t *block_tables, int max_blocks_per_seq, const int *prefix_lens,
                      const int *chunk_lens, int num_seqs, int num_heads, int num_kv_heads, int head_dim,
-                     int block_size, int num_blocks, float scale, pa_dtype dtype, int *d_err, void *stream) {
+                     int block_size, int num_blocks, float scale, pa_dtype dtype, void *workspace,
+                     size_t workspace_bytes, int *d_err, void *stream) {
     if (num_seqs < 0 || num_heads <= 0 || num_kv_heads <= 0 || head_dim <= 0 || block_size <= 0 ||
         num_blocks <= 0 || max_blocks_per_seq <= 0 || !good_dtype(dtype))
         return PA_ERR_INVALID_ARG;
@@ -395,6 +406,7 @@ int pa_prefill_batch(void *out, const void *query, const void *k_cache, const vo
     p.num_blocks = num_blocks;
     p.scale_log2 = scale * 1.4426950408889634f;
     // sequences with a non-empty chunk, kPrefillMaxSeqs per launch
+    p.query_rows = (int)rows;
     int row = 0;
     for (int i = 0; i < num_seqs; ++i) {
         if (chunk_lens[i] > 0) {
@@ -406,8 +418,8 @@ int pa_prefill_batch(void *out, const void *query, const void *k_cache, const vo
         }
         row += chunk_lens[i];
         if (p.num_seqs == pa::kPrefillMaxSeqs || (i == num_seqs - 1 && p.num_seqs > 0)) {
-            const int rc = pa::launch_prefill(dtype, head_dim, block_size, num_heads / num_kv_heads, p,
-                                              static_cast<cudaStream_t>(stream));
+            const int rc = pa::launch_prefill(dtype, head_dim, block_size, num_heads / num_kv_heads, p, workspace,
+                                              workspace_bytes, static_cast<cudaStream_t>(stream));
             if (rc != PA_OK) return rc;
             p.num_seqs = 0;
         }
@@ -586,8 +598,8 @@ int pa_mixed_step(void *prefill_out, const void *prefill_query, const int32_t *p
         // one half only: no fork
         int rc = pa_prefill_batch(prefill_out, prefill_query, k_cache, v_cache, prefill_block_tables,
                                   num_prefill ? prefill_max_blocks : 1, prefix_lens, chunk_lens, num_prefill,
-                                  num_heads, num_kv_heads, head_dim, block_size, num_blocks, scale, dtype, d_err,
-                                  stream);
+                                  num_heads, num_kv_heads, head_dim, block_size, num_blocks, scale, dtype, nullptr, 0,
+                                  d_err, stream);
         if (rc != PA_OK) return rc;
         return pa_decode(decode_out, decode_query, k_cache, v_cache, decode_block_tables,
                          num_decode ? decode_max_blocks : 1, context_lens, num_decode, num_heads, num_kv_heads,
@@ -606,7 +618,8 @@ int pa_mixed_step(void *prefill_out, const void *prefill_query, const int32_t *p
         return PA_ERR_CUDA;
     const int rc_pf = pa_prefill_batch(prefill_out, prefill_query, k_cache, v_cache, prefill_block_tables,
                                        prefill_max_blocks, prefix_lens, chunk_lens, num_prefill, num_heads,
-                                       num_kv_heads, head_dim, block_size, num_blocks, scale, dtype, d_err, f->stream);
+                                       num_kv_heads, head_dim, block_size, num_blocks, scale, dtype, nullptr, 0, d_err,
+                                       f->stream);
     const int rc_dec = pa_decode(decode_out, decode_query, k_cache, v_cache, decode_block_tables, decode_max_blocks,
                                  context_lens, num_decode, num_heads, num_kv_heads, head_dim, block_size,
                                  num_blocks, max_context_len, scale, partition_tokens, dtype, workspace,

@@ -66,12 +66,17 @@ struct DecodeParams {
     int red_fixed_slots;         // reduce: slots before the per-sequence ones
 };
 
-// One sequence's chunk in a batched prefill launch.
+// One sequence's chunk in a prefill launch.  Its work units are (kv head,
+// row tile of 256 query rows); their key tiles are laid end to end after the
+// previous sequences' (the launcher fills in the schedule fields).
 struct PrefillSeq {
     const int32_t *block_table;  // [>= ceil((prefix_len+chunk_len)/bs)]
     int prefix_len, chunk_len;
     int row_start;               // first row of the chunk in query/out
-    int cta_start;               // first CTA (grid x) of the sequence; a multiple of the cluster size
+    int row_tiles;               // row tiles of the chunk (ceil(chunk_len * group / 256))
+    int tiles_per_head;          // key tiles of all its row tiles for one kv head
+    int tile_start;              // global index of its first key tile
+    int unit_start;              // global index of its first unit
 };
 
 constexpr int kPrefillMaxSeqs = 64;  // sequences per launch (kernel-parameter table)
@@ -85,7 +90,13 @@ struct PrefillParams {
     int num_heads, num_kv_heads, num_blocks;
     float scale_log2;
     int num_seqs;                // entries of seqs in use (1 .. kPrefillMaxSeqs)
-    int num_ctas;                // grid x: cta_start of a sequence past the last
+    int query_rows;              // rows of query/out (all chunks of the call, across launches)
+    int total_tiles;             // key tiles of all units
+    int split;                   // 1: stream-K ranges over gridDim.x CTAs, with merging; 0: one unit per CTA
+    float *part_o;               // split: [2 * CTAs][2 Q tiles][128 rows][128] unnormalised O of partial units
+    float2 *part_ml;             // split: [2 * CTAs][2 Q tiles][128 rows] (running max, sum)
+    unsigned *counters;          // split: [units][2 Q tiles] segments counted so far; zero on entry, and
+                                 // the merging segment resets its unit's to zero before the call ends
     PrefillSeq seqs[kPrefillMaxSeqs];
 };
 
@@ -115,7 +126,11 @@ size_t copy_blocks_workspace_bytes(int num_pairs);
 int launch_copy_blocks(void *k_cache, void *v_cache, const int64_t *pairs, int num_pairs,
                        int num_kv_heads, int head_dim, int block_size, int num_blocks, void *workspace,
                        int *d_err, cudaStream_t stream);
+// Workspace for the stream-K prefill schedule (an upper bound for any batch of
+// num_seqs chunks totalling total_chunk_len rows).
+size_t prefill_workspace_bytes(int num_seqs, long long total_chunk_len, int group, int num_kv_heads);
+// workspace may be NULL (or too small): each CTA then computes one whole unit.
 int launch_prefill(pa_dtype dt, int head_dim, int block_size, int group, const PrefillParams &p,
-                   cudaStream_t stream);
+                   void *workspace, size_t workspace_bytes, cudaStream_t stream);
 
 }  // namespace pa

@@ -122,7 +122,13 @@ def test_cache_calls_reject_bad_arguments_on_host(lib):
     assert lib.pa_copy_blocks(buf, buf, buf, 3, 2, 128, 16, 64, 1, buf, ws - 1, None, None) == -5
     assert lib.pa_copy_blocks(buf, buf, buf, 3, 2, 128, 16, 64, 1, p((1 << 20) + 8), ws, None, None) == -6
     assert lib.pa_copy_blocks(buf, buf, buf, (1 << 26) + 1, 2, 128, 16, 64, 1, buf, 1 << 40, None, None) == -3
-    assert lib.pa_prefill_chunk(buf, buf, buf, buf, buf, 8, 4, 7, 2, 128, 16, 64, 0.1, 1, None, None) == -1
+    assert lib.pa_prefill_chunk(buf, buf, buf, buf, buf, 8, 4, 7, 2, 128, 16, 64, 0.1, 1, None, 0, None, None) == -1
+    # a workspace too small for the stream-K schedule, or misaligned (both found before any CUDA call)
+    assert lib.pa_prefill_chunk(buf, buf, buf, buf, buf, 8, 4, 8, 2, 128, 16, 64, 0.1, 1, buf, 16, None, None) == -5
+    need = lib.pa_prefill_workspace_bytes(1, 4, 8, 2, 128)
+    assert need > 0 and lib.pa_prefill_workspace_bytes(1, 4, 7, 2, 128) == 0
+    assert lib.pa_prefill_chunk(buf, buf, buf, buf, buf, 8, 4, 8, 2, 128, 16, 64, 0.1, 1, p((1 << 20) + 16), need,
+                                None, None) == -6
 
 
 def test_shared_prefix_and_batch_prefill_reject_bad_arguments_on_host(lib):
@@ -150,7 +156,7 @@ def test_shared_prefix_and_batch_prefill_reject_bad_arguments_on_host(lib):
 
     def pb(prefix=pl, chunk=cl, n=3, Hq=4, Hkv=2, scale=0.1, mb=4):
         return lib.pa_prefill_batch(buf, buf, buf, buf, buf, mb, prefix, chunk, n, Hq, Hkv, 128, 16, 64,
-                                    f(scale), 1, None, None)
+                                    f(scale), 1, None, 0, None, None)
     assert pb(chunk=bad) == -1                 # negative chunk length
     assert pb(chunk=big) == -3                 # prefix + chunk past the table row
     assert pb(Hq=3) == -1

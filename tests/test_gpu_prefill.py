@@ -31,13 +31,17 @@ def _built():
     g.build()
 
 
-def run_prefill(case, t):
+def run_prefill(case, t, split=True):
+    """Cache write then prefill; ``split``: with a workspace (stream-K over one
+    CTA per SM, partial units merged), else one CTA per unit."""
     err = torch.zeros(1, dtype=torch.int32, device=DEV)
     pa.pa_reshape_and_cache(t["new_key"], t["new_value"], t["k_cache"], t["v_cache"],
                             torch.as_tensor(case.slot_mapping, device=DEV), d_err=err)
     out = torch.full_like(t["query"], float("nan"))
+    ws = pa.prefill_workspace(t["query"], case.num_kv_heads) if split else None
     pa.pa_prefill_chunk(out, t["query"], t["k_cache"], t["v_cache"],
-                        torch.as_tensor(case.block_table, device=DEV), case.prefix_len, case.scale, d_err=err)
+                        torch.as_tensor(case.block_table, device=DEV), case.prefix_len, case.scale, d_err=err,
+                        workspace=ws)
     torch.cuda.synchronize()
     assert int(err.item()) == 0, f"device error flags {int(err.item()):#x}"
     return out
@@ -56,8 +60,9 @@ CASES = [
 ]
 
 
+@pytest.mark.parametrize("split", [True, False])
 @pytest.mark.parametrize("P,C,G,Hkv,bs,dtype", CASES)
-def test_prefill_chunk_matches_oracle(P, C, G, Hkv, bs, dtype):
+def test_prefill_chunk_matches_oracle(P, C, G, Hkv, bs, dtype, split):
     case = wl.make_prefill_case(f"pf{P}_{C}", P, C, G * Hkv, Hkv, 128, bs, dtype, seed=P + 7 * C + G)
     t = case.materialize(DEV)
     kc, vc = wl.bits(t["k_cache"]), wl.bits(t["v_cache"])
@@ -65,8 +70,32 @@ def test_prefill_chunk_matches_oracle(P, C, G, Hkv, bs, dtype):
                                     case.slot_mapping, bs) == 0
     ref = oracle.prefill_chunk(wl.bits(t["query"]), kc, vc, case.block_table, P, case.scale, dtype,
                                num_threads=8)
-    out = run_prefill(case, t)
+    out = run_prefill(case, t, split)
     check_attention(to_f64(out), ref, dtype, case.name)
+
+
+@pytest.mark.parametrize("P,C,G,Hkv,bs,dtype", [
+    (8000, 32, 8, 1, 16, "bf16"),    # one unit of 64 key tiles over 64 CTAs: one tile each, 64 partials merged
+    (0, 256, 1, 2, 16, "f16"),       # 2 units of 2 tiles over 4 CTAs: rows 0-127 see nothing in the second tile
+    (300, 40, 4, 3, 32, "bf16"),     # units of 3 tiles, ranges of one or two tiles
+    (5000, 700, 8, 2, 16, "bf16"),   # 22 units, several cut
+])
+def test_prefill_split_units_merge_to_the_oracle(P, C, G, Hkv, bs, dtype):
+    # stream-K ranges cut units into segments whose partials are merged by
+    # the last one to finish; some segments hold no visible key for some rows
+    case = wl.make_prefill_case(f"pfsplit{P}_{C}", P, C, G * Hkv, Hkv, 128, bs, dtype, seed=11 + P + C)
+    t = case.materialize(DEV, pool_fill=float("nan"))
+    kc, vc = wl.bits(t["k_cache"]), wl.bits(t["v_cache"])
+    assert oracle.reshape_and_cache(wl.bits(t["new_key"]), wl.bits(t["new_value"]), kc, vc,
+                                    case.slot_mapping, bs) == 0
+    ref = oracle.prefill_chunk(wl.bits(t["query"]), kc, vc, case.block_table, P, case.scale, dtype,
+                               num_threads=8)
+    out = run_prefill(case, t, split=True)
+    assert torch.isfinite(out.float()).all()
+    check_attention(to_f64(out), ref, dtype, case.name)
+    # the merge follows key order, not arrival order: a second run gives the same bits
+    again = run_prefill(case, t, split=True)
+    assert torch.equal(out, again)
 
 
 def test_prefill_full_size_every_row():
@@ -83,10 +112,12 @@ def test_prefill_full_size_every_row():
     assert oracle.reshape_and_cache(wl.bits(t["new_key"]), wl.bits(t["new_value"]), kc, vc, slots,
                                     case.block_size) == 0
     q = wl.bits(t["query"])
-    out = run_prefill(case, t)
+    out = run_prefill(case, t)          # the benchmark's schedule: stream-K with a workspace
     ref = oracle.prefill_chunk(q, kc, vc, compact, case.prefix_len, case.scale, case.dtype,
                                num_threads=os.cpu_count() or 8)
     check_attention(to_f64(out), ref, case.dtype, case.name)
+    whole = run_prefill(case, t, split=False)
+    check_attention(to_f64(whole), ref, case.dtype, case.name + " one CTA per unit")
 
 
 @pytest.mark.parametrize("chunks,bs", [([512, 512, 512, 512], 16), ([700, 13, 1335], 16),
@@ -109,6 +140,7 @@ def test_prompt_prefilled_chunk_after_chunk(chunks, bs):
     bt = torch.as_tensor(case.block_table, device=DEV)
     err = torch.zeros(1, dtype=torch.int32, device=DEV)
     out = torch.full_like(t["query"], float("nan"))
+    ws = pa.prefill_workspace(t["query"], case.num_kv_heads)
     a = 0
     for c in chunks:
         b = a + c
@@ -116,7 +148,7 @@ def test_prompt_prefilled_chunk_after_chunk(chunks, bs):
                                 t["v_cache"], slots[a:b].contiguous(), d_err=err)
         part = torch.full_like(t["query"][a:b], float("nan"))
         pa.pa_prefill_chunk(part, t["query"][a:b].contiguous(), t["k_cache"], t["v_cache"], bt, a, case.scale,
-                            d_err=err)
+                            d_err=err, workspace=ws)
         out[a:b] = part
         a = b
     torch.cuda.synchronize()
@@ -191,13 +223,14 @@ def _oracle_batch(case, t):
     return refs
 
 
-def _gpu_batch(case, t):
+def _gpu_batch(case, t, split=False):
     err = torch.zeros(1, dtype=torch.int32, device=DEV)
     pa.pa_reshape_and_cache(t["new_key"], t["new_value"], t["k_cache"], t["v_cache"],
                             torch.as_tensor(case.slot_mapping, device=DEV), d_err=err)
     out = torch.full_like(t["query"], float("nan"))
+    ws = pa.prefill_workspace(t["query"], case.num_kv_heads, len(case.chunk_lens)) if split else None
     pa.pa_prefill_batch(out, t["query"], t["k_cache"], t["v_cache"], torch.as_tensor(case.block_tables, device=DEV),
-                        case.prefix_lens, case.chunk_lens, case.scale, d_err=err)
+                        case.prefix_lens, case.chunk_lens, case.scale, d_err=err, workspace=ws)
     torch.cuda.synchronize()
     assert int(err.item()) == 0, f"device error flags {int(err.item()):#x}"
     return out
@@ -208,10 +241,14 @@ def test_prefill_batch_matches_oracle_and_single_calls(P, C, G, Hkv, bs, dtype):
     case = wl.make_prefill_batch_case(f"pfb{len(P)}", P, C, G * Hkv, Hkv, 128, bs, dtype, seed=sum(P) + sum(C))
     t = case.materialize(DEV)
     refs = _oracle_batch(case, t)
+    split = _gpu_batch(case, t, split=True)
+    for row, ref in refs:
+        check_attention(to_f64(split[row:row + ref.shape[0]]), ref, dtype, f"{case.name} stream-K row {row}")
     out = _gpu_batch(case, t)
     for row, ref in refs:
         check_attention(to_f64(out[row:row + ref.shape[0]]), ref, dtype, f"{case.name} row {row}")
-    # each sequence's rows equal a pa_prefill_chunk call on that sequence alone, bit for bit
+    # without a workspace each sequence's rows equal a pa_prefill_chunk call
+    # on that sequence alone (also without one), bit for bit
     row = 0
     for i, (p_, c_) in enumerate(zip(case.prefix_lens.tolist(), case.chunk_lens.tolist())):
         if c_:
@@ -231,15 +268,16 @@ def test_prefill_batch_beyond_one_launch():
     case = wl.make_prefill_batch_case("pfb70", P, C, 8, 2, 128, 16, "bf16", seed=70)
     t = case.materialize(DEV)
     refs = _oracle_batch(case, t)
-    out = _gpu_batch(case, t)
-    for row, ref in refs:
-        check_attention(to_f64(out[row:row + ref.shape[0]]), ref, "bf16", f"row {row}")
+    for split in (False, True):
+        out = _gpu_batch(case, t, split=split)
+        for row, ref in refs:
+            check_attention(to_f64(out[row:row + ref.shape[0]]), ref, "bf16", f"row {row} split {split}")
 
 
 def test_prefill_batch_full_size_sampled_rows():
     case = wl.prefill_batch_case()
     t = case.materialize(DEV)
-    out = _gpu_batch(case, t)
+    out = _gpu_batch(case, t, split=True)
     assert torch.isfinite(out.float()).all()
     # sampled rows of two sequences against the oracle (a row is a decode at P+r+1)
     kc, vc = wl.bits(t["k_cache"]), wl.bits(t["v_cache"])
@@ -314,5 +352,5 @@ def test_prefill_random_shapes(i, P, C, G, Hkv, bs, dtype):
     assert oracle.reshape_and_cache(wl.bits(t["new_key"]), wl.bits(t["new_value"]), kc, vc,
                                     case.slot_mapping, bs) == 0
     ref = oracle.prefill_chunk(wl.bits(t["query"]), kc, vc, case.block_table, P, case.scale, dtype, num_threads=8)
-    out = run_prefill(case, t)
+    out = run_prefill(case, t, split=i % 2 == 0)
     check_attention(to_f64(out), ref, dtype, case.name)
