@@ -89,6 +89,9 @@ constexpr int kThreads = 64 + kQT * 128;
 // as 128 packed pairs), O of each Q tile (128 fp32)
 constexpr uint32_t kColS = 0, kColO = 256;
 constexpr uint32_t kTmemCols = 512;
+// Hardware barriers: 1 + g over Q tile g's softmax warps (merging), kBarP + g
+// over those warps and the MMA warp (P of Q tile g written)
+constexpr int kBarP = 3;
 
 // Key tiles of row tile r of sequence q: up to the last key its last row sees.
 __host__ __device__ __forceinline__ int unit_tiles(int prefix_len, int chunk_len, int G, int r) {
@@ -301,11 +304,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint64_t *q_full = bars + 2 * kSlots;       // TMA -> MMA (both Q tiles of a segment landed)
     uint64_t *q_empty = q_full + 1;             // softmax (Q tile 1) -> TMA (the segment's last QKs finished)
     uint64_t *s_full = q_empty + 1;             // [kQT] MMA -> softmax (S ready, O holds all PVs before it)
-    uint64_t *p_full = s_full + kQT;            // [kQT] softmax -> MMA (S read, P written, O rescaled)
-    uint64_t *o_done = p_full + kQT;            // [kQT] MMA -> softmax (last PV of the segment finished)
+    uint64_t *o_done = s_full + kQT;            // [kQT] MMA -> softmax (last PV of the segment finished)
     volatile uint32_t *tmem_holder = reinterpret_cast<volatile uint32_t *>(o_done + kQT);
     volatile int *merge_flag = reinterpret_cast<volatile int *>(tmem_holder + 1);  // [kQT]
-    static_assert((2 * kSlots + 2 + 3 * kQT) * 8 + 4 + 4 * kQT <= kSmemUsed - kOffBar, "barrier area");
+    static_assert((2 * kSlots + 2 + 2 * kQT) * 8 + 4 + 4 * kQT <= kSmemUsed - kOffBar, "barrier area");
 
     pdl_wait();  // the kernel before this one on the stream (the chunk's cache write) has finished
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -330,7 +332,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_init(q_empty, 1);
         for (int g = 0; g < kQT; ++g) {
             mbar_init(&s_full[g], 1);
-            mbar_init(&p_full[g], 128);
             mbar_init(&o_done[g], 1);
         }
         fence_barrier_init();
@@ -426,7 +427,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int i = max(0, nitems - kSlots); i < nitems; ++i) mbar_wait(&full[i % kSlots], (uint32_t)(i / kSlots) & 1u);
     } else if (warp == 1) {
         // ============================================================ MMA issuer
-        if (lane == 0) {
+        // One thread issues; the whole warp takes the P announcements, which
+        // come through hardware barriers (kBarP + g, the four softmax warps of
+        // Q tile g arrive, this warp syncs) rather than mbarriers: a wait on an
+        // mbarrier costs the issuing thread a few hundred cycles even when the
+        // phase is long complete.
+        {
             constexpr uint32_t idesc_qk = instr_desc(kBf16, false, false, kM, kNK);
             constexpr uint32_t idesc_pv = instr_desc(kBf16, false, true, kM, kD);
             constexpr uint32_t hi_q = desc_hi(1024);   // Q: 8-row groups 1 KB apart
@@ -440,14 +446,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int x = x0, sc = 0; x < x1; ++sc) {
                 const Seg sg = seg_at<G>(p, x, x1);
                 const int nt = sg.t1 - sg.t0;
-                wait_or_flag(q_full, (uint32_t)sc & 1u, p.d_err);
+                if (lane == 0) wait_or_flag(q_full, (uint32_t)sc & 1u, p.d_err);
                 for (int k = 0; k <= nt; ++k) {
                     const int gt = tc + k;  // this CTA's tile count
                     const int sl_v = (2 * gt - 1) % kSlots, sl_k = (2 * gt) % kSlots;
-                    // K of a segment's first tile is the only copy this thread
+                    // K of a segment's first tile is the only copy this warp
                     // waits for: Q tile 0's softmax announces P(j) only once
                     // V(j) and K(j+1) have landed
-                    if (k == 0) {
+                    if (k == 0 && lane == 0) {
                         wait_or_flag(&full[sl_k], (uint32_t)(2 * gt / kSlots) & 1u, p.d_err);
                         tc_fence_after();
                     }
@@ -456,16 +462,19 @@ __global__ void __launch_bounds__(kThreads, 1)
                         const uint32_t tS = tmem + kColS + g * kNK;
                         if (k >= 1) {
                             // O_g += P_g(k-1) V(k-1); P sits in S_g's first 64 columns
-                            wait_or_flag(&p_full[g], (uint32_t)(gt - 1) & 1u, p.d_err);
-                            tc_fence_after();
-                            const uint32_t v_lo = v_lo0 + sl_v * (kKVTile >> 4);
+                            __syncwarp();
+                            named_bar_sync(kBarP + g, 160);
+                            if (lane == 0) {
+                                tc_fence_after();
+                                const uint32_t v_lo = v_lo0 + sl_v * (kKVTile >> 4);
 #pragma unroll
-                            for (int kk = 0; kk < kNK / 16; ++kk)
-                                mma_f16_ts(tmem + kColO + g * kD, tS + kk * 8,
-                                           desc_of(v_lo + kk * (4096 >> 4), hi_kv), idesc_pv, k > 1 || kk > 0);
-                            if (k == nt) mma_commit(&o_done[g]);
+                                for (int kk = 0; kk < kNK / 16; ++kk)
+                                    mma_f16_ts(tmem + kColO + g * kD, tS + kk * 8,
+                                               desc_of(v_lo + kk * (4096 >> 4), hi_kv), idesc_pv, k > 1 || kk > 0);
+                                if (k == nt) mma_commit(&o_done[g]);
+                            }
                         }
-                        if (k < nt) {
+                        if (k < nt && lane == 0) {
                             // S_g = Q_g K(k)^T
                             const uint32_t q_lo = q_lo0 + g * (kQTile >> 4);
                             const uint32_t k_lo = k_lo0 + sl_k * (kKVTile >> 4);
@@ -578,13 +587,17 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                     for (int c = 0; c < kNK; ++c) s[c] = (kb + c <= plim) ? s[c] : -INFINITY;
                 }
+                // row max with three-input maxima: 8 chains over the 128 columns
                 float mx8[8];
 #pragma unroll
-                for (int e = 0; e < 8; ++e) mx8[e] = s[e];
+                for (int e = 0; e < 8; ++e) mx8[e] = fmaxf(s[e], s[8 + e]);
+                static_assert(kNK % 16 == 0, "columns in steps of 16");
 #pragma unroll
-                for (int c = 8; c < kNK; ++c) mx8[c & 7] = fmaxf(mx8[c & 7], s[c]);
-                float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
-                                 fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
+                for (int c = 16; c < kNK; c += 16) {
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) mx8[e] = fmax3(mx8[e], s[c + e], s[c + 8 + e]);
+                }
+                float mx = fmax3(fmax3(mx8[0], mx8[1], mx8[2]), fmax3(mx8[3], mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7]));
                 mx *= csc;
 
                 // Lazy rescale: the maximum moves only when it grew by more than
@@ -664,7 +677,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 tmem_wait_st();
                 tc_fence_before();
-                mbar_arrive1(&p_full[g]);
+                named_bar_arrive(kBarP + g, 160);
             }
 
             // ---- end of the segment.  O (unnormalised) is complete in TMEM; it
