@@ -273,25 +273,41 @@ PA_API int pa_decode_step_host(void *out_host, const void *query_host, const voi
 
 /*
  * pa_mixed_step -- one continuous-batching step over one pool: the prompt
- * chunks of num_prefill sequences (exactly pa_prefill_batch) and one decode
- * token for each of num_decode other sequences (exactly pa_decode), run
- * concurrently.  The chunks' kernel goes first, on a high-priority stream the
- * library forks from `stream` and joins back into it, so its CTAs are placed
- * first; the decode streams KV over the SMs the chunks leave free (a prompt
- * chunk's tensor-core CTAs need a whole SM's shared memory and tensor memory
- * and cannot share one with decode CTAs) and takes every SM as the chunks
- * finish.  The pages' chunked prefill, whose point is to batch prompt chunks
- * with decodes ("vLLM PagedAttention chuyen sau" (locionic.com), "Chunked
- * Prefill").  Both halves read the pool as it is when the call is reached
- * on `stream`: write the step's new K/V first (pa_reshape_and_cache).
+ * chunks of num_prefill sequences (as pa_prefill_batch) and one decode token
+ * for each of num_decode other sequences (as pa_decode), together.  The
+ * pages' chunked prefill, whose point is to batch prompt chunks with decodes
+ * ("vLLM PagedAttention chuyen sau" (locionic.com), "Chunked Prefill",
+ * mechanism steps 2 and 4).  Both halves read the pool as it is when the call
+ * is reached on `stream`: write the step's new K/V first (pa_reshape_and_cache).
  * Arguments as for pa_prefill_batch (prefill_*, prefix_lens, chunk_lens on
- * the host) and pa_decode (decode_*, context_lens on the device, workspace),
- * with the pool and the model shape shared.  A half with no sequences is
- * skipped (no fork).  The fork stream and its two events are created on the
- * first call on a device and kept; calls from several host threads are
- * serialised around the fork.  Returns the first failing half's status
- * (the other half may have been queued; the join is always queued).
+ * the host) and pa_decode (decode_*, context_lens on the device), with the
+ * pool and the model shape shared.
+ *
+ * One launch: with head_dim 128, 8 query heads per kv head, block_size 16 to
+ * 128, max_context_len <= 16384, at most 64 non-empty chunks, and a
+ * workspace of at least pa_mixed_step_workspace_bytes(...) bytes, 256-byte
+ * aligned and ZERO-FILLED before its first use, the step is one kernel of one
+ * CTA per SM: some CTAs run the chunks (the stream-K prefill over those
+ * CTAs), the others decode (sequence, kv head) units drawn from a queue the
+ * whole grid shares (one partition each, so no reduce), and the chunks' CTAs
+ * join the queue when their share of the chunks is done; the split of the
+ * SMs follows the chunks' key tiles and the decodes' estimated K/V bytes, so
+ * the tensor cores and HBM work at the same time.  The calls leave the
+ * workspace's counters at zero, so one workspace serves every later step
+ * whose sizes it covers; two steps must not run on one workspace at the same
+ * time.  Results equal the separate calls' up to rounding.
+ * Two launches otherwise (or when the workspace is smaller, e.g. only
+ * pa_decode's): the chunks' kernel first on a high-priority stream the library
+ * forks from `stream` and joins back into it, the decode on `stream` over the
+ * SMs the chunks leave free; the workspace is then pa_decode's.  The fork
+ * stream and its two events are created on the first such call on a device
+ * and kept; calls from several host threads are serialised around the fork.
+ * A half with no sequences is skipped.  Returns the first failing half's
+ * status (the other half may have been queued).
  */
+PA_API size_t pa_mixed_step_workspace_bytes(int num_prefill, int total_chunk_len, int num_decode, int num_heads,
+                                            int num_kv_heads, int head_dim, int block_size, int max_context_len,
+                                            int partition_tokens);
 PA_API int pa_mixed_step(void *prefill_out, const void *prefill_query, const int32_t *prefill_block_tables,
                          int prefill_max_blocks, const int *prefix_lens, const int *chunk_lens, int num_prefill,
                          void *decode_out, const void *decode_query, const int32_t *decode_block_tables,

@@ -30,7 +30,7 @@ EXPORTED = ("pa_status_string", "pa_reshape_and_cache", "pa_decode_partition_tok
             "pa_bm_create", "pa_bm_destroy", "pa_bm_add_sequence", "pa_bm_fork", "pa_bm_append_token",
             "pa_bm_free_sequence", "pa_bm_block_table", "pa_bm_seq_len", "pa_bm_block_refcount",
             "pa_bm_stats", "pa_prefill_batch", "pa_decode_step_host_staging_bytes", "pa_decode_step_host",
-            "pa_mixed_step", "pa_bounded_wait_polls", "pa_selftest_bounded_wait")
+            "pa_mixed_step", "pa_mixed_step_workspace_bytes", "pa_bounded_wait_polls", "pa_selftest_bounded_wait")
 PA_ERR_NO_BLOCKS = -8
 PA_ERR_SCRATCH_LIMIT = -7
 NOALLOC_SCRATCH_BYTES = 64 << 20
@@ -112,6 +112,8 @@ def lib() -> ctypes.CDLL:
         L.pa_mixed_step.argtypes = [p, p, p, i, p, p, i, p, p, p, i, p, i, i, i, p, sz, p, p, i, i, i, i, i,
                                     ctypes.c_float, i, p, p]
         L.pa_mixed_step.restype = i
+        L.pa_mixed_step_workspace_bytes.argtypes = [i] * 9
+        L.pa_mixed_step_workspace_bytes.restype = sz
         L.pa_bounded_wait_polls.argtypes = []
         L.pa_bounded_wait_polls.restype = i
         L.pa_selftest_bounded_wait.argtypes = [i, p, p, p]
@@ -323,9 +325,12 @@ def pa_decode_step_host(out, query, new_key, new_value, slot_mapping, block_tabl
 def pa_mixed_step(prefill_out, prefill_query, prefill_block_tables, prefix_lens, chunk_lens, decode_out,
                   decode_query, decode_block_tables, context_lens, k_cache, v_cache, scale, max_context_len,
                   partition_tokens=0, workspace=None, d_err=None, stream=None):
-    """One continuous-batching step: ``pa_prefill_batch`` over the prompt
-    chunks and ``pa_decode`` over the decoding sequences, run concurrently.
-    prefix_lens / chunk_lens are host int sequences; the rest as for those calls."""
+    """One continuous-batching step: the prompt chunks (as ``pa_prefill_batch``)
+    and the decoding sequences (as ``pa_decode``) together, in one launch when
+    the shape allows (see include/pa.h), else two concurrent ones.
+    prefix_lens / chunk_lens are host int sequences; the rest as for those calls.
+    ``workspace``: from ``mixed_workspace`` (zero-filled; reuse it across steps),
+    or None to allocate one here."""
     _dev(prefill_out, prefill_query, prefill_block_tables, decode_out, decode_query, decode_block_tables,
          context_lens, k_cache, v_cache, workspace, d_err)
     for bt in (prefill_block_tables, decode_block_tables, context_lens):
@@ -345,7 +350,7 @@ def pa_mixed_step(prefill_out, prefill_query, prefill_block_tables, prefix_lens,
             v_cache.dtype):
         raise TypeError("dtype mismatch")
     if workspace is None:
-        workspace = decode_workspace(decode_query, Hkv, bs, max_context_len, partition_tokens)
+        workspace = mixed_workspace(prefill_query, decode_query, Hkv, bs, n, max_context_len, partition_tokens)
     rc = lib().pa_mixed_step(
         _ptr(prefill_out), _ptr(prefill_query), _ptr(prefill_block_tables), prefill_block_tables.shape[1],
         P.ctypes.data_as(ctypes.c_void_p), C.ctypes.data_as(ctypes.c_void_p), n, _ptr(decode_out),
@@ -354,6 +359,17 @@ def pa_mixed_step(prefill_out, prefill_query, prefill_block_tables, prefix_lens,
         _ptr(k_cache), _ptr(v_cache), Hq, Hkv, D, bs, NB, float(scale), _dt(decode_query), _ptr(d_err),
         _stream(k_cache, stream))
     _check("pa_mixed_step", rc)
+
+
+def mixed_workspace(prefill_query, decode_query, num_kv_heads, block_size, num_prefill, max_context_len,
+                    partition_tokens=0):
+    """A zero-filled uint8 CUDA workspace for ``pa_mixed_step`` (zero-filled
+    once; the calls keep it usable)."""
+    R, Hq, D = prefill_query.shape
+    B = decode_query.shape[0]
+    n = int(lib().pa_mixed_step_workspace_bytes(int(num_prefill), R, B, Hq, int(num_kv_heads), D, int(block_size),
+                                                int(max_context_len), int(partition_tokens)))
+    return torch.zeros(max(n, 1), dtype=torch.uint8, device=decode_query.device)
 
 
 def pa_selftest_bounded_wait(max_polls, d_err, d_cycles=None, stream=None):

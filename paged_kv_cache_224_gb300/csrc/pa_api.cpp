@@ -582,6 +582,126 @@ int fork_stream(ForkStream **out) {
     return PA_OK;
 }
 
+// Longest context the fused step decodes as one partition per sequence.
+constexpr int kMixedMaxContext = 16384;
+
+// The fused step's workspace: the decode's split-K region (used when the step
+// runs as two launches), then the stream-K prefill region, which must stay
+// zero-filled between calls (the decode region never overlaps it).
+size_t mixed_decode_region(int num_decode, int num_heads, int num_kv_heads, int head_dim, int block_size,
+                           int max_context_len, int partition_tokens) {
+    if (num_decode <= 0) return 0;
+    const size_t d = pa_decode_workspace_bytes(num_decode, num_heads, num_kv_heads, head_dim, block_size,
+                                               max_context_len, partition_tokens);
+    return round256(d);
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t pa_mixed_step_workspace_bytes(int num_prefill, int total_chunk_len, int num_decode, int num_heads,
+                                     int num_kv_heads, int head_dim, int block_size, int max_context_len,
+                                     int partition_tokens) {
+    if (num_prefill < 0 || total_chunk_len < 0 || num_decode < 0 || num_heads <= 0 || num_kv_heads <= 0 ||
+        num_heads % num_kv_heads || head_dim <= 0 || block_size <= 0 || max_context_len < 0)
+        return 0;
+    const size_t dec = mixed_decode_region(num_decode, num_heads, num_kv_heads, head_dim, block_size,
+                                           max_context_len, partition_tokens);
+    const size_t pre = num_prefill > 0 ? pa_prefill_workspace_bytes(num_prefill, total_chunk_len, num_heads,
+                                                                    num_kv_heads, head_dim)
+                                       : 0;
+    return dec + pre;
+}
+
+}  // extern "C"
+
+namespace {
+
+// The step as one launch (pa::launch_mixed) when the shape allows it; returns
+// PA_ERR_UNSUPPORTED (having queued nothing) when it does not.
+int mixed_fused(void *prefill_out, const void *prefill_query, const int32_t *prefill_block_tables,
+                int prefill_max_blocks, const int *prefix_lens, const int *chunk_lens, int num_prefill,
+                void *decode_out, const void *decode_query, const int32_t *decode_block_tables, int decode_max_blocks,
+                const int32_t *context_lens, int num_decode, int max_context_len, int partition_tokens,
+                void *workspace, size_t workspace_bytes, const void *k_cache, const void *v_cache, int num_heads,
+                int num_kv_heads, int head_dim, int block_size, int num_blocks, float scale, pa_dtype dtype,
+                int *d_err, void *stream) {
+    const int group = num_heads / num_kv_heads;
+    if (!pa::mixed_supported(head_dim, block_size, group) || max_context_len > kMixedMaxContext ||
+        max_context_len <= 0 || !workspace || !good_dtype(dtype))
+        return PA_ERR_UNSUPPORTED;
+    if (!std::isfinite(scale) || !(scale > 0.f)) return PA_ERR_UNSUPPORTED;
+    if (!prefill_out || !prefill_query || !prefill_block_tables || !prefix_lens || !chunk_lens || !decode_out ||
+        !decode_query || !decode_block_tables || !context_lens || !k_cache || !v_cache)
+        return PA_ERR_UNSUPPORTED;
+    if (!aligned16(prefill_out) || !aligned16(prefill_query) || !aligned16(decode_out) ||
+        !aligned16(decode_query) || !aligned16(k_cache) || !aligned16(v_cache))
+        return PA_ERR_UNSUPPORTED;
+    if (prefill_max_blocks <= 0 || decode_max_blocks <= 0 || num_blocks <= 0) return PA_ERR_UNSUPPORTED;
+    // the prompt chunks, one launch's worth
+    pa::PrefillParams pp{};
+    pp.out = prefill_out;
+    pp.query = prefill_query;
+    pp.k_cache = k_cache;
+    pp.v_cache = v_cache;
+    pp.d_err = d_err;
+    pp.num_heads = num_heads;
+    pp.num_kv_heads = num_kv_heads;
+    pp.num_blocks = num_blocks;
+    pp.scale_log2 = scale * 1.4426950408889634f;
+    long long rows = 0;
+    int row = 0;
+    for (int i = 0; i < num_prefill; ++i) {
+        if (prefix_lens[i] < 0 || chunk_lens[i] < 0) return PA_ERR_UNSUPPORTED;
+        if ((long long)prefix_lens[i] + chunk_lens[i] > (long long)prefill_max_blocks * block_size)
+            return PA_ERR_UNSUPPORTED;
+        if (chunk_lens[i] > 0) {
+            if (pp.num_seqs == pa::kPrefillMaxSeqs) return PA_ERR_UNSUPPORTED;
+            pa::PrefillSeq &q = pp.seqs[pp.num_seqs++];
+            q.block_table = prefill_block_tables + (size_t)i * prefill_max_blocks;
+            q.prefix_len = prefix_lens[i];
+            q.chunk_len = chunk_lens[i];
+            q.row_start = row;
+        }
+        row += chunk_lens[i];
+        rows += chunk_lens[i];
+    }
+    if (pp.num_seqs == 0 || rows > 0x7fffffffLL) return PA_ERR_UNSUPPORTED;
+    pp.query_rows = (int)rows;
+    // the decodes, one partition per sequence
+    pa::DecodeParams dp{};
+    dp.out = decode_out;
+    dp.query = decode_query;
+    dp.k_cache = k_cache;
+    dp.v_cache = v_cache;
+    dp.block_tables = decode_block_tables;
+    dp.context_lens = context_lens;
+    dp.d_err = d_err;
+    dp.num_seqs = num_decode;
+    dp.num_heads = num_heads;
+    dp.num_kv_heads = num_kv_heads;
+    dp.max_blocks_per_seq = decode_max_blocks;
+    dp.num_blocks = num_blocks;
+    dp.max_context_len = max_context_len;
+    dp.block_size = block_size;
+    dp.partition_tokens = (max_context_len + block_size - 1) / block_size * block_size;
+    dp.max_partitions = 1;
+    dp.scale_log2 = pp.scale_log2;
+    dp.grp_size = 1;
+    dp.grp_inner = group;
+    dp.table_stride = decode_max_blocks;
+    dp.slots = 1;
+    const size_t dec = mixed_decode_region(num_decode, num_heads, num_kv_heads, head_dim, block_size, max_context_len,
+                                           partition_tokens);
+    if (workspace_bytes <= dec) return PA_ERR_UNSUPPORTED;
+    // the decodes' K/V bytes, estimated from the longest context (lengths are on the device)
+    const double decode_bytes = (double)num_decode * num_kv_heads * (0.5 * max_context_len) * head_dim * 2 * 2;
+    const int rc = pa::launch_mixed(dtype, block_size, group, pp, dp, static_cast<char *>(workspace) + dec,
+                                    workspace_bytes - dec, decode_bytes, static_cast<cudaStream_t>(stream));
+    return rc == PA_ERR_WORKSPACE || rc == PA_ERR_ALIGNMENT ? PA_ERR_UNSUPPORTED : rc;
+}
+
 }  // namespace
 
 extern "C" {
@@ -605,6 +725,15 @@ int pa_mixed_step(void *prefill_out, const void *prefill_query, const int32_t *p
                          num_decode ? decode_max_blocks : 1, context_lens, num_decode, num_heads, num_kv_heads,
                          head_dim, block_size, num_blocks, max_context_len, scale, partition_tokens, dtype,
                          workspace, workspace_bytes, d_err, stream);
+    }
+    {
+        // one launch when the shape and the workspace allow it
+        const int rc = mixed_fused(prefill_out, prefill_query, prefill_block_tables, prefill_max_blocks, prefix_lens,
+                                   chunk_lens, num_prefill, decode_out, decode_query, decode_block_tables,
+                                   decode_max_blocks, context_lens, num_decode, max_context_len, partition_tokens,
+                                   workspace, workspace_bytes, k_cache, v_cache, num_heads, num_kv_heads, head_dim,
+                                   block_size, num_blocks, scale, dtype, d_err, stream);
+        if (rc != PA_ERR_UNSUPPORTED) return rc;
     }
     std::lock_guard<std::mutex> guard(g_fork_mutex);
     ForkStream *f = nullptr;

@@ -100,6 +100,17 @@ struct PrefillParams {
     PrefillSeq seqs[kPrefillMaxSeqs];
 };
 
+// One launch of a continuous-batching step: CTAs 0 .. prefill_ctas-1 run the
+// prompt chunks (the stream-K prefill over those CTAs), the others the decodes
+// as a persistent role (one partition per sequence, so no reduce).
+struct MixedParams {
+    PrefillParams pp;
+    DecodeParams dp;
+    int prefill_ctas;
+    int decode_units;            // sequences x kv heads
+    unsigned *decode_next;       // the decode CTAs' shared unit queue (0 between launches)
+};
+
 // Split-K partition length for the automatic setting.
 int auto_partition_tokens(int num_seqs, int num_heads, int num_kv_heads, int block_size, int max_context_len);
 
@@ -132,5 +143,14 @@ size_t prefill_workspace_bytes(int num_seqs, long long total_chunk_len, int grou
 // workspace may be NULL (or too small): each CTA then computes one whole unit.
 int launch_prefill(pa_dtype dt, int head_dim, int block_size, int group, const PrefillParams &p,
                    void *workspace, size_t workspace_bytes, cudaStream_t stream);
+// Whether launch_mixed has a kernel for these (head_dim 128, a tensor-core
+// decode group, block_size 16..128).
+bool mixed_supported(int head_dim, int block_size, int group);
+// The fused step: pp as for launch_prefill (at most kPrefillMaxSeqs chunks),
+// dp as for launch_decode with one partition per sequence; prefill_ws as for
+// launch_prefill (required); decode_bytes: the decodes' K/V bytes, estimated,
+// to split the SMs between the two halves.
+int launch_mixed(pa_dtype dt, int block_size, int group, const PrefillParams &pp, const DecodeParams &dp,
+                 void *workspace, size_t workspace_bytes, double decode_bytes, cudaStream_t stream);
 
 }  // namespace pa

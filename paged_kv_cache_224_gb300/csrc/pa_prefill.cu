@@ -63,6 +63,7 @@
 
 #include <type_traits>
 
+#include "pa_decode_tc.cuh"
 #include "pa_device.cuh"
 #include "pa_internal.h"
 #include "pa_tcgen05.cuh"
@@ -285,10 +286,13 @@ __device__ __noinline__ void finish_partial(float4 *part_o, float2 *part_ml, uns
 
 // ---- the kernel ------------------------------------------------------------
 
-template <typename T, int BS, int G>
-__global__ void __launch_bounds__(kThreads, 1)
-    prefill_tc_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap tmk,
-                      const __grid_constant__ CUtensorMap tmv, const __grid_constant__ CUtensorMap tmq) {
+// The prefill work of CTA `cta` of `ncta`: with the stream-K schedule, its
+// share of the key tiles; without, unit `cta` (all of the CTA's threads call this).
+// Returns the CTA's TMEM base; with kKeepTmem (the one-launch step, whose
+// prefill CTAs go on to decode) the allocation is left for the caller to free.
+template <typename T, int BS, int G, bool kKeepTmem = false>
+__device__ __forceinline__ uint32_t prefill_cta(const PrefillParams &p, const CUtensorMap &tmk,
+                                                const CUtensorMap &tmv, const CUtensorMap &tmq, int cta, int ncta) {
     constexpr bool kBf16 = std::is_same<T, __nv_bfloat16>::value;
     constexpr int kBlocksPerTile = kNK / BS;
     static_assert(kNK % BS == 0 && BS % 8 == 0 && 32 % kBlocksPerTile == 0, "block_size");
@@ -309,17 +313,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     volatile int *merge_flag = reinterpret_cast<volatile int *>(tmem_holder + 1);  // [kQT]
     static_assert((2 * kSlots + 2 + 2 * kQT) * 8 + 4 + 4 * kQT <= kSmemUsed - kOffBar, "barrier area");
 
-    pdl_wait();  // the kernel before this one on the stream (the chunk's cache write) has finished
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
     // this CTA's key tiles [x0, x1) of the global order
     int x0, x1;
-    const long long W = p.total_tiles, N = gridDim.x;
+    const long long W = p.total_tiles, N = ncta;
     if (p.split) {
-        x0 = (int)(W * blockIdx.x / N);
-        x1 = (int)(W * (blockIdx.x + 1) / N);
+        x0 = (int)(W * cta / N);
+        x1 = (int)(W * (cta + 1) / N);
     } else {
-        unit_range<G>(p, (int)blockIdx.x, x0, x1);
+        unit_range<G>(p, cta, x0, x1);
     }
     const int nitems = 2 * (x1 - x0);  // ring items: K and V of every tile
 
@@ -492,7 +495,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 x += nt;
             }
         }
-    } else {
+    } else if (warp < 2 + 4 * kQT) {  // (a wider CTA's other warps only meet the final barrier)
         // ============================================================ softmax
         const int g = (warp - 2) >> 2;         // Q tile of this warp group
         const int quarter = warp & 3;          // TMEM lanes 32*quarter .. +31 (fixed by the warp id)
@@ -702,10 +705,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                     // part of a unit: write the partial to this CTA's slot (0 for
                     // the first segment of its range, 1 for the last), count it,
                     // and if it is the unit's last to arrive, merge all of them
-                    const long long Wt = p.total_tiles, Nc = gridDim.x;
+                    const long long Wt = p.total_tiles, Nc = ncta;
                     finish_partial<T>(reinterpret_cast<float4 *>(p.part_o), p.part_ml, &p.counters[sg.unit * kQT + g],
-                                      orow, rw.valid, tO, tS, x_next >= x1, g, t, 2 * (int)blockIdx.x + (sc == 0 ? 0 : 1),
-                                      (int)blockIdx.x, cta_of(sg.x_unit, Wt, Nc), cta_of(sg.x_unit + sg.n - 1, Wt, Nc),
+                                      orow, rw.valid, tO, tS, x_next >= x1, g, t, 2 * cta + (sc == 0 ? 0 : 1),
+                                      cta, cta_of(sg.x_unit, Wt, Nc), cta_of(sg.x_unit + sg.n - 1, Wt, Nc),
                                       sg.x_unit, Wt, Nc, m_run, l_run, merge_flag);
                 }
             }
@@ -715,11 +718,73 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     tc_fence_before();
     __syncthreads();
-    if (warp == 1) {
+    if (!kKeepTmem && warp == 1) {
         tc_fence_after();
         asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols)
                      : "memory");
     }
+    return tmem;
+}
+
+template <typename T, int BS, int G>
+__global__ void __launch_bounds__(kThreads, 1)
+    prefill_tc_kernel(const __grid_constant__ PrefillParams p, const __grid_constant__ CUtensorMap tmk,
+                      const __grid_constant__ CUtensorMap tmv, const __grid_constant__ CUtensorMap tmq) {
+    pdl_wait();  // the kernel before this one on the stream (the chunk's cache write) has finished
+    prefill_cta<T, BS, G>(p, tmk, tmv, tmq, (int)blockIdx.x, (int)gridDim.x);
+}
+
+// ---- one launch of a continuous-batching step --------------------------------
+//
+// Every CTA runs two decode instances of six warps each, every instance the
+// tensor-core decode's pipeline (its own three-slot ring, TMEM columns and
+// softmax barrier) over units (sequence, kv head) drawn one after another from
+// a queue the grid shares; CTAs 0 .. prefill_ctas-1 first run the prompt
+// chunks exactly as the prefill kernel (stream-K over those CTAs; the two
+// extra warps wait at its final barrier) and join the queue when their range
+// is done.  Two instances keep as many K/V bytes in flight on an SM as two
+// standalone decode CTAs, and the shared queue spreads long and short
+// contexts, and the SMs the prompt chunks free, over the decodes as they go.
+// The prefill CTAs keep the tensor cores busy while the decode CTAs stream
+// K/V from HBM, in one grid of one CTA per SM, so neither half waits for the
+// other to release SMs.
+constexpr int kMixedThreads = kThreads + 64;  // twelve warps: two decode instances
+constexpr int kDecodeSlotsMixed = tcd::kSlotsStandalone;
+constexpr uint32_t kDecodeInst1 = (tcd::TcLayout<kDecodeSlotsMixed>::kSmemUsed + 1023u) & ~1023u;
+constexpr uint32_t kMixedHolder = kOffBar + 248;  // TMEM base of a decode-only CTA (past the prefill's barriers)
+static_assert(kMixedThreads == 2 * tcd::kThreads, "two decode instances");
+static_assert(kDecodeInst1 + tcd::TcLayout<kDecodeSlotsMixed>::kSmemUsed <= (uint32_t)kOffBar,
+              "both decode instances fit below the prefill's barriers");
+static_assert((2 * kSlots + 2 + 2 * kQT) * 8 + 4 + 4 * kQT <= 248, "the holder is past the prefill's barriers");
+static_assert(2 * tcd::kTmemCols <= kTmemCols, "both instances' columns in the prefill's allocation");
+
+template <typename T, int BS, int G>
+__global__ void __launch_bounds__(kMixedThreads, 1)
+    mixed_tc_kernel(const __grid_constant__ MixedParams mp, const __grid_constant__ CUtensorMap tmk,
+                    const __grid_constant__ CUtensorMap tmv, const __grid_constant__ CUtensorMap tmq) {
+    const bool prefill = (int)blockIdx.x < mp.prefill_ctas;
+    const int warp = threadIdx.x >> 5, inst = (int)threadIdx.x / tcd::kThreads;
+    extern __shared__ unsigned char smem_raw[];
+    const uint32_t raw = smem_addr(smem_raw);
+    volatile uint32_t *holder =
+        reinterpret_cast<volatile uint32_t *>(smem_raw + (((raw + 1023u) & ~1023u) - raw) + kMixedHolder);
+    uint32_t tmem = 0;
+    if (prefill)  // ends with a CTA barrier: every warp is past the prefill's use of shared memory and TMEM
+        tmem = prefill_cta<T, BS, G, true>(mp.pp, tmk, tmv, tmq, (int)blockIdx.x, mp.prefill_ctas);
+    tcd::TcRun r;
+    tcd::tc_init<kDecodeSlotsMixed>(r, inst * kDecodeInst1, inst * 6, 5 + inst);
+    if (!prefill && warp == 1) tcd::tc_alloc(holder, 2 * tcd::kTmemCols);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (!prefill) tmem = *holder;
+    r.tmem = tmem + inst * tcd::kTmemCols;
+    tcd::tc_queue_loop<T, BS, G, kDecodeSlotsMixed>(mp.dp, &tmk, &tmv, r, mp.decode_next, mp.decode_units,
+                                                    2 * (int)gridDim.x);
+    tcd::tc_drain<kDecodeSlotsMixed>(r);
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) tcd::tc_dealloc(tmem, prefill ? (uint32_t)kTmemCols : 2 * tcd::kTmemCols);
 }
 
 // ---- host side -------------------------------------------------------------
@@ -796,14 +861,22 @@ int launch_tc_dtype(int block_size, int group, const PrefillParams &p, unsigned 
 size_t round256(size_t n) { return (n + 255) / 256 * 256; }
 
 // Workspace regions for `ctas` stream-K CTAs and `units` merge counters.
+// [ctas][2 slots][kQT][128 rows][128] partial outputs, [ctas][2][kQT][128]
+// (max, sum) pairs, 256 bytes holding the one-launch step's decode queue
+// counter, then a counter per (unit, Q tile).  Only the counters' length
+// depends on the call, so every counter sits at the same place from call to
+// call and stays zero between calls.
 struct PrefillWs {
-    size_t o_bytes, ml_bytes, cnt_bytes;
-    size_t total() const { return o_bytes + ml_bytes + cnt_bytes; }
+    size_t o_bytes, ml_bytes, q_bytes, cnt_bytes;
+    size_t queue_off() const { return o_bytes + ml_bytes; }
+    size_t cnt_off() const { return o_bytes + ml_bytes + q_bytes; }
+    size_t total() const { return o_bytes + ml_bytes + q_bytes + cnt_bytes; }
 };
 PrefillWs prefill_ws(long long ctas, long long units) {
     PrefillWs w;
     w.o_bytes = round256((size_t)ctas * 2 * kQT * kM * kD * sizeof(float));
     w.ml_bytes = round256((size_t)ctas * 2 * kQT * kM * sizeof(float2));
+    w.q_bytes = 256;
     w.cnt_bytes = round256((size_t)units * kQT * sizeof(unsigned));
     return w;
 }
@@ -816,15 +889,11 @@ size_t prefill_workspace_bytes(int num_seqs, long long total_chunk_len, int grou
     return prefill_ws(sm_count(), units).total();
 }
 
-int launch_prefill(pa_dtype dt, int head_dim, int block_size, int group, const PrefillParams &p_in,
-                   void *workspace, size_t workspace_bytes, cudaStream_t stream) {
-    if (head_dim != kD) return PA_ERR_UNSUPPORTED;
-    // TMA row coordinates are 32-bit
-    if ((long long)p_in.num_blocks * p_in.num_kv_heads * block_size >= (1LL << 31)) return PA_ERR_UNSUPPORTED;
-    if (p_in.num_seqs < 1 || p_in.num_seqs > kPrefillMaxSeqs) return PA_ERR_INVALID_ARG;
-    if (group < 1 || kM % group) return PA_ERR_UNSUPPORTED;
-    // units in (sequence, kv head, row tile) order and their key tiles laid end to end
-    PrefillParams p = p_in;
+namespace {
+
+// Units in (sequence, kv head, row tile) order and their key tiles laid end to
+// end: fills the schedule fields of p.  Returns PA_OK, or an error.
+int prefill_schedule(PrefillParams &p, int group, long long *units_out) {
     long long tiles = 0, units = 0;
     for (int i = 0; i < p.num_seqs; ++i) {
         PrefillSeq &q = p.seqs[i];
@@ -841,8 +910,26 @@ int launch_prefill(pa_dtype dt, int head_dim, int block_size, int group, const P
         units += (long long)row_tiles * p.num_kv_heads;
         if (tiles > 0x3fffffffLL || units > 0x3fffffffLL) return PA_ERR_UNSUPPORTED;
     }
-    if (units == 0) return PA_OK;
     p.total_tiles = (int)tiles;
+    *units_out = units;
+    return PA_OK;
+}
+
+}  // namespace
+
+int launch_prefill(pa_dtype dt, int head_dim, int block_size, int group, const PrefillParams &p_in,
+                   void *workspace, size_t workspace_bytes, cudaStream_t stream) {
+    if (head_dim != kD) return PA_ERR_UNSUPPORTED;
+    // TMA row coordinates are 32-bit
+    if ((long long)p_in.num_blocks * p_in.num_kv_heads * block_size >= (1LL << 31)) return PA_ERR_UNSUPPORTED;
+    if (p_in.num_seqs < 1 || p_in.num_seqs > kPrefillMaxSeqs) return PA_ERR_INVALID_ARG;
+    if (group < 1 || kM % group) return PA_ERR_UNSUPPORTED;
+    PrefillParams p = p_in;
+    long long units = 0;
+    const int rc = prefill_schedule(p, group, &units);
+    if (rc != PA_OK) return rc;
+    if (units == 0) return PA_OK;
+    const long long tiles = p.total_tiles;
     const long long ctas = std::min<long long>(sm_count(), tiles);
     // The layout depends on the device only (partial regions for one CTA per
     // SM, counters after them), never on the call: the counters must stay put
@@ -865,7 +952,7 @@ int launch_prefill(pa_dtype dt, int head_dim, int block_size, int group, const P
         p.part_ml = reinterpret_cast<float2 *>(base + ws.o_bytes);
         // zero on entry: the caller zero-fills the workspace once, and the
         // segment that merges a unit resets its counter before the call ends
-        p.counters = reinterpret_cast<unsigned *>(base + ws.o_bytes + ws.ml_bytes);
+        p.counters = reinterpret_cast<unsigned *>(base + ws.cnt_off());
         grid = (unsigned)ctas;
     } else {
         p.split = 0;
@@ -873,6 +960,100 @@ int launch_prefill(pa_dtype dt, int head_dim, int block_size, int group, const P
     }
     return dt == PA_BF16 ? launch_tc_dtype<__nv_bfloat16>(block_size, group, p, grid, stream)
                          : launch_tc_dtype<__half>(block_size, group, p, grid, stream);
+}
+
+namespace {
+
+template <typename T, int BS, int G>
+int launch_mixed_t(const MixedParams &mp, unsigned grid, cudaStream_t stream) {
+    auto kern = mixed_tc_kernel<T, BS, G>;
+    static std::atomic<uint64_t> attr_done{0};
+    if (ensure_smem_attr(kern, kSmemAlloc, attr_done) != PA_OK) return PA_ERR_CUDA;
+    const bool bf16 = std::is_same<T, __nv_bfloat16>::value;
+    CUtensorMap tmk, tmv, tmq;
+    if (!make_pool_map(&tmk, mp.pp.k_cache, mp.pp, BS, bf16) || !make_pool_map(&tmv, mp.pp.v_cache, mp.pp, BS, bf16) ||
+        !make_query_map(&tmq, mp.pp, G, bf16))
+        return PA_ERR_CUDA;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(kMixedThreads);
+    cfg.dynamicSmemBytes = kSmemAlloc;
+    cfg.stream = stream;
+    // launched in plain stream order: launched early behind the cache write
+    // (which lets dependents start at once), the step measured about 0.17 ms
+    // slower, its CTAs starting that much later
+    return cudaLaunchKernelEx(&cfg, kern, mp, tmk, tmv, tmq) == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+}
+
+template <typename T>
+int launch_mixed_dtype(int block_size, int group, const MixedParams &mp, unsigned grid, cudaStream_t stream) {
+    if (group != 8) return PA_ERR_UNSUPPORTED;
+    switch (block_size) {
+        case 16: return launch_mixed_t<T, 16, 8>(mp, grid, stream);
+        case 32: return launch_mixed_t<T, 32, 8>(mp, grid, stream);
+        case 64: return launch_mixed_t<T, 64, 8>(mp, grid, stream);
+        case 128: return launch_mixed_t<T, 128, 8>(mp, grid, stream);
+        default: return PA_ERR_UNSUPPORTED;
+    }
+}
+
+// Time model of one CTA per SM, to split the SMs between the halves: a prefill
+// CTA finishes a 128-key tile of 256 rows in about 1.7 us (plus 5% for the
+// static schedule's stragglers); a decode CTA streams about 61 GB/s, and all
+// of them together about 6.4 TB/s; once the prefill CTAs are done they join
+// the decode.  The split minimises the step; the count of prefill CTAs is even
+// (the CTAs pair up on the SM pairs of a TPC: with an odd count the one
+// prefill CTA that shared its pair with a decode CTA ran about a third longer
+// than the rest).
+int mixed_prefill_ctas(long long prefill_tiles, double decode_bytes, int sms) {
+    int best = 2;
+    double best_t = 1e30;
+    for (int n = 2; n < sms; n += 2) {
+        const double tp = (double)prefill_tiles * 1.7e-6 * 1.05 / n;
+        const double cap = 6.4e12;
+        const double bw = std::min(cap, (sms - n) * 61e9);
+        const double t = decode_bytes <= tp * bw ? std::max(tp, decode_bytes / bw)
+                                                 : tp + (decode_bytes - tp * bw) / cap;
+        if (t < best_t) {
+            best_t = t;
+            best = n;
+        }
+    }
+    return best;
+}
+
+}  // namespace
+
+bool mixed_supported(int head_dim, int block_size, int group) {
+    return head_dim == kD && group == 8 && (block_size == 16 || block_size == 32 || block_size == 64 || block_size == 128);
+}
+
+int launch_mixed(pa_dtype dt, int block_size, int group, const PrefillParams &pp_in, const DecodeParams &dp,
+                 void *workspace, size_t workspace_bytes, double decode_bytes, cudaStream_t stream) {
+    if (!mixed_supported(kD, block_size, group)) return PA_ERR_UNSUPPORTED;
+    if ((long long)pp_in.num_blocks * pp_in.num_kv_heads * block_size >= (1LL << 31)) return PA_ERR_UNSUPPORTED;
+    if (pp_in.num_seqs < 1 || pp_in.num_seqs > kPrefillMaxSeqs) return PA_ERR_INVALID_ARG;
+    MixedParams mp{};
+    mp.pp = pp_in;
+    mp.dp = dp;
+    long long units = 0;
+    const int rc = prefill_schedule(mp.pp, group, &units);
+    if (rc != PA_OK) return rc;
+    const int sms = sm_count();
+    if (units == 0 || sms < 2) return PA_ERR_UNSUPPORTED;
+    const PrefillWs ws = prefill_ws(sms, units);
+    if (!workspace || workspace_bytes < ws.total()) return PA_ERR_WORKSPACE;
+    if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return PA_ERR_ALIGNMENT;
+    char *base = static_cast<char *>(workspace);
+    mp.pp.split = 1;
+    mp.pp.part_o = reinterpret_cast<float *>(base);
+    mp.pp.part_ml = reinterpret_cast<float2 *>(base + ws.o_bytes);
+    mp.pp.counters = reinterpret_cast<unsigned *>(base + ws.cnt_off());
+    mp.decode_next = reinterpret_cast<unsigned *>(base + ws.queue_off());
+    mp.prefill_ctas = (int)std::min<long long>(mixed_prefill_ctas(mp.pp.total_tiles, decode_bytes, sms), mp.pp.total_tiles);
+    mp.decode_units = dp.num_seqs * dp.num_kv_heads;
+    return dt == PA_BF16 ? launch_mixed_dtype<__nv_bfloat16>(block_size, group, mp, (unsigned)sms, stream)
+                         : launch_mixed_dtype<__half>(block_size, group, mp, (unsigned)sms, stream);
 }
 
 }  // namespace pa

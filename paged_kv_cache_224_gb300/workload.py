@@ -451,13 +451,28 @@ class MixedCase:
         tot = sum(C * P + C * (C + 1) // 2 for P, C in zip(self.prefix_lens.tolist(), self.chunk_lens.tolist()))
         return 4 * self.head_dim * tot * self.num_heads
 
-    def materialize(self, device="cpu") -> dict:
+    def materialize(self, device="cpu", pool_fill: Optional[float] = None) -> dict:
+        """``pool_fill`` replaces every pool slot past each sequence's context
+        (decode: position L-1; prompt chunk: P+C-1) and every unused block with
+        this constant (e.g. NaN: nothing past a context may reach an output)."""
         g = torch.Generator(device=device)
         g.manual_seed(self.seed)
         dt = TORCH_DTYPES[self.dtype]
         Hq, Hkv, D = self.num_heads, self.num_kv_heads, self.head_dim
         kc = torch.randn((self.num_blocks, Hkv, self.block_size, D), generator=g, device=device, dtype=dt)
         vc = torch.randn((self.num_blocks, Hkv, self.block_size, D), generator=g, device=device, dtype=dt)
+        if pool_fill is not None:
+            bs = self.block_size
+            owned = torch.zeros((self.num_blocks, bs), dtype=torch.bool)
+            ends = [(self.decode_tables[i], int(L)) for i, L in enumerate(self.context_lens)]
+            ends += [(self.prefill_tables[i], int(P + C)) for i, (P, C) in
+                     enumerate(zip(self.prefix_lens.tolist(), self.chunk_lens.tolist()))]
+            for table, end in ends:
+                for j in range(blocks_for(end, bs)):
+                    owned[int(table[j]), :min(bs, end - j * bs)] = True
+            mask = (~owned).to(device)[:, None, :, None].expand_as(kc)
+            kc[mask] = pool_fill
+            vc[mask] = pool_fill
         dq = torch.randn((self.num_seqs, Hq, D), generator=g, device=device, dtype=dt)
         pq = torch.randn((int(self.chunk_lens.sum()), Hq, D), generator=g, device=device, dtype=dt)
         T = int(self.slot_mapping.shape[0])

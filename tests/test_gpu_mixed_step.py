@@ -1,12 +1,17 @@
 """One continuous-batching step (pa_mixed_step): prompt chunks and decodes
-over one pool, run concurrently.
+over one pool, together.
 
 The pages' chunked prefill batches prompt chunks with the decodes of other
 sequences (page "vLLM PagedAttention chuyen sau", section "Chunked
-Prefill").  The concurrent step must give, bit for bit, what the two calls
-give one after the other (the same kernels on the same inputs), and both
-halves must match the oracle.
+Prefill").  With 8 query heads per kv head the step is one launch (prefill
+CTAs and persistent decode CTAs in one grid): both halves must match the
+oracle, two steps in a row must give the same bits (the workspace is reused),
+and garbage past the contexts must not leak in.  Otherwise (other groups, or
+a workspace sized only for pa_decode) the step is two concurrent launches and
+must give, bit for bit, what the two calls give one after the other.
 """
+import os
+
 import numpy as np
 import pytest
 import torch
@@ -37,14 +42,34 @@ def device_args(case):
             torch.as_tensor(case.context_lens, device=DEV))
 
 
-def mixed(case, t, err, pt=0):
+def mixed(case, t, err, pt=0, workspace=None):
     pbt, dbt, lens = device_args(case)
     pout = torch.full_like(t["prefill_query"], float("nan"))
     dout = torch.full_like(t["decode_query"], float("nan"))
     pa.pa_mixed_step(pout, t["prefill_query"], pbt, case.prefix_lens, case.chunk_lens, dout, t["decode_query"], dbt,
                      lens, t["k_cache"], t["v_cache"], case.scale, case.max_context_len, partition_tokens=pt,
-                     d_err=err)
+                     workspace=workspace, d_err=err)
     return pout, dout
+
+
+def two_launch_workspace(case, t, pt=0):
+    # sized for pa_decode only: the step runs as two concurrent launches
+    return pa.decode_workspace(t["decode_query"], case.num_kv_heads, case.block_size, case.max_context_len, pt)
+
+
+def check_both_halves(c, t, pm, dm, what):
+    kc, vc = wl.bits(t["k_cache"]), wl.bits(t["v_cache"])
+    ref_d = oracle.decode(wl.bits(t["decode_query"]), kc, vc, c.decode_tables, c.context_lens, c.scale, c.dtype,
+                          num_threads=os.cpu_count() or 8)
+    check_attention(to_f64(dm), ref_d, c.dtype, f"{what}: decode half")
+    q = wl.bits(t["prefill_query"])
+    row = 0
+    for i, (P, C) in enumerate(zip(c.prefix_lens.tolist(), c.chunk_lens.tolist())):
+        if C:
+            ref_p = oracle.prefill_chunk(q[row:row + C], kc, vc, c.prefill_tables[i], P, c.scale, c.dtype,
+                                         num_threads=os.cpu_count() or 8)
+            check_attention(to_f64(pm[row:row + C]), ref_p, c.dtype, f"{what}: prefill seq {i}")
+        row += C
 
 
 def separate(case, t, err, pt=0):
@@ -60,12 +85,13 @@ def separate(case, t, err, pt=0):
 
 @pytest.mark.parametrize("G,dtype", [(4, "bf16"), (8, "f16"), (1, "bf16")])
 def test_mixed_step_equals_the_two_calls_and_the_oracle(G, dtype):
+    # two concurrent launches (a workspace sized for pa_decode only)
     c = wl.make_mixed_case(f"mixed_g{G}", [1, 300, 2049, 0, 700, 129], [40, 0, 333], [9, 17, 130], 2 * G, 2, 128,
                            16, dtype, seed=80 + G)
     t = c.materialize(DEV)
     err = torch.zeros(1, dtype=torch.int32, device=DEV)
     write_step_kv(c, t, err)
-    pm, dm = mixed(c, t, err, pt=256)
+    pm, dm = mixed(c, t, err, pt=256, workspace=two_launch_workspace(c, t, 256))
     ps, ds = separate(c, t, err, pt=256)
     torch.cuda.synchronize()
     assert int(err.item()) == 0
@@ -82,27 +108,79 @@ def test_mixed_step_equals_the_two_calls_and_the_oracle(G, dtype):
         row += C
 
 
-def test_mixed_step_full_size_equals_the_two_calls():
+@pytest.mark.parametrize("prefix,chunks,lens,bs,dtype", [
+    ([40, 0, 333], [9, 17, 130], [1, 300, 2049, 0, 700, 129], 16, "f16"),
+    ([1000, 5], [64, 700], [5000, 1, 17, 2048, 128, 4097], 32, "bf16"),
+    ([0], [1], [3], 16, "bf16"),
+    ([8192], [512], [int(x) for x in np.random.default_rng(3).integers(1, 4097, size=40)], 16, "bf16"),
+])
+def test_mixed_step_one_launch_matches_the_oracle(prefix, chunks, lens, bs, dtype):
+    # one launch (8 query heads per kv head, a mixed-step workspace): every
+    # output of both halves against the oracle; two steps in a row give the
+    # same bits with the same workspace; NaN past every context stays out
+    c = wl.make_mixed_case("mixed1", lens, prefix, chunks, 16, 2, 128, bs, dtype, seed=sum(lens) % 1000)
+    t = c.materialize(DEV, pool_fill=float("nan"))
+    err = torch.zeros(1, dtype=torch.int32, device=DEV)
+    write_step_kv(c, t, err)
+    ws = pa.mixed_workspace(t["prefill_query"], t["decode_query"], c.num_kv_heads, bs, len(chunks), c.max_context_len)
+    pm, dm = mixed(c, t, err, workspace=ws)
+    pm2, dm2 = mixed(c, t, err, workspace=ws)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0, f"device error flags {int(err.item()):#x}"
+    assert torch.equal(pm, pm2) and torch.equal(dm, dm2)
+    check_both_halves(c, t, pm, dm, "one launch")
+
+
+def test_mixed_step_one_launch_workspace_shared_by_steps_of_other_shapes():
+    # the decode queue's counter and the stream-K counters live in the
+    # workspace and must be back at zero after every step, whatever its shape:
+    # steps A, B, A, B on one workspace give the bits of A and B run alone
+    a = wl.make_mixed_case("mixed_a", [int(x) for x in np.random.default_rng(5).integers(0, 3000, size=300)],
+                           [700], [200], 16, 2, 128, 16, "bf16", seed=7)
+    b = wl.make_mixed_case("mixed_b", [5, 1, 4000], [0, 64], [300, 17], 16, 2, 128, 16, "bf16", seed=8)
+    ta, tb = a.materialize(DEV), b.materialize(DEV)
+    err = torch.zeros(1, dtype=torch.int32, device=DEV)
+    write_step_kv(a, ta, err)
+    write_step_kv(b, tb, err)
+    # sized for the larger half of each (B's 317 chunk rows, A's 300 decodes)
+    fresh = lambda: pa.mixed_workspace(tb["prefill_query"], ta["decode_query"], 2, 16, 2, 4096)
+    ws = fresh()
+    pa1, da1 = mixed(a, ta, err, workspace=fresh())
+    pb1, db1 = mixed(b, tb, err, workspace=fresh())
+    runs = [mixed(c, t, err, workspace=ws) for c, t in ((a, ta), (b, tb), (a, ta), (b, tb))]
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    for (pm, dm), (pr, dr) in zip(runs, [(pa1, da1), (pb1, db1)] * 2):
+        assert torch.equal(pm, pr) and torch.equal(dm, dr)
+    check_both_halves(a, ta, pa1, da1, "step A")
+    check_both_halves(b, tb, pb1, db1, "step B")
+
+
+def test_mixed_step_full_size_one_launch_matches_the_oracle_and_two_launches_match_the_calls():
     c = wl.mixed_case()
     t = c.materialize(DEV)
     err = torch.zeros(1, dtype=torch.int32, device=DEV)
     write_step_kv(c, t, err)
-    pm, dm = mixed(c, t, err)
+    pm, dm = mixed(c, t, err)                       # one launch
+    p2, d2 = mixed(c, t, err, workspace=two_launch_workspace(c, t))
     ps, ds = separate(c, t, err)
     torch.cuda.synchronize()
     assert int(err.item()) == 0
-    assert torch.equal(pm, ps) and torch.equal(dm, ds)
-    assert torch.isfinite(pm.float()).all() and torch.isfinite(dm.float()).all()
+    assert torch.equal(p2, ps) and torch.equal(d2, ds)
+    check_both_halves(c, t, pm, dm, "full size, one launch")
 
 
-def test_mixed_step_replays_from_a_cuda_graph():
-    # the fork onto the library's stream and the join back must survive capture
+@pytest.mark.parametrize("one_launch", [False, True])
+def test_mixed_step_replays_from_a_cuda_graph(one_launch):
+    # two launches: the fork onto the library's stream and the join back must
+    # survive capture; one launch: the kernel replays with the same bits
     c = wl.make_mixed_case("mixed_graph", [1, 300, 2049, 700], [100], [64], 8, 2, 128, 16, "bf16", seed=90)
     t = c.materialize(DEV)
     err = torch.zeros(1, dtype=torch.int32, device=DEV)
     pbt, dbt, lens = device_args(c)
     slots = torch.as_tensor(c.slot_mapping, device=DEV)  # no host copies inside the capture
-    ws = pa.decode_workspace(t["decode_query"], 2, 16, c.max_context_len, 256)
+    ws = (pa.mixed_workspace(t["prefill_query"], t["decode_query"], 2, 16, len(c.chunk_lens), c.max_context_len, 256)
+          if one_launch else two_launch_workspace(c, t, 256))
     pout = torch.empty_like(t["prefill_query"])
     dout = torch.empty_like(t["decode_query"])
 
