@@ -41,9 +41,11 @@
 //             A operand; the tensor pipe runs one thread's MMAs in order, so
 //             the PV of tile j-1 has read P before the QK of tile j writes S,
 //             and S_g(j) being complete means O_g holds every PV up to j-1.
-//             Every wait or commit costs this thread a few hundred cycles in
-//             which it issues nothing, so it waits only for P (one wait per Q
-//             tile and key tile) and commits only S and the last PV;
+//             Every mbarrier wait or commit costs this thread a few hundred
+//             cycles in which it issues nothing, so it commits only S and the
+//             last PV, and learns that P is written and that the copies have
+//             landed through hardware barriers the other warps arrive on or
+//             sync with;
 //   warps 2-5 softmax of Q tile 0, warps 6-9 of Q tile 1: each thread owns one
 //             query row = one TMEM lane; it reads its whole S row (one TMEM
 //             wait), applies the causal mask, updates the running max
@@ -51,13 +53,14 @@
 //             writes P (rounded to the input type) into TMEM, and at the end
 //             of the segment stores the normalised row or its partial.  The
 //             two groups interleave, so the tensor pipe works on one Q tile's
-//             MMAs while the other's softmax runs.  Q tile 0's threads also
-//             wait, before announcing P(j), for the V(j) and K(j+1) copies the
-//             next MMAs read, and Q tile 1's hand K(j) and V(j-1)'s ring slots
-//             back to the producer once S_1(j) is complete (every MMA before
-//             it has finished).  On the unit's last key tile each group zeroes
-//             the V rows past the unit's last key, so garbage (even NaN) in
-//             unused slots never reaches O.
+//             MMAs while the other's softmax runs.  Q tile 1's threads hand
+//             K(j) and V(j-1)'s ring slots back to the producer once S_1(j) is
+//             complete (every MMA before it has finished).  On the unit's last
+//             key tile each group zeroes the V rows past the unit's last key,
+//             so garbage (even NaN) in unused slots never reaches O;
+//   warp 10   load watcher: per key tile j, waits for the V(j) and K(j+1)
+//             copies and then syncs with the MMA warp before it issues the PV
+//             of tile j and the QK of tile j+1.
 // All waits are bounded; a wait that gives up flags PA_DEVERR_TIMEOUT.
 #include <cuda.h>
 
@@ -85,7 +88,7 @@ constexpr int kOffKV = kOffQ + kQT * kQTile;               // 64 KB: K/V ring
 constexpr int kOffBar = kOffKV + kSlots * kKVTile;         // 224 KB
 constexpr int kSmemUsed = kOffBar + 256;
 constexpr int kSmemAlloc = kSmemUsed + 1024;               // room to align the base to 1 KB
-constexpr int kThreads = 64 + kQT * 128;
+constexpr int kThreads = 64 + kQT * 128 + 32;
 // TMEM columns: S of each Q tile (128 fp32; P overwrites its first 64 columns
 // as 128 packed pairs), O of each Q tile (128 fp32)
 constexpr uint32_t kColS = 0, kColO = 256;
@@ -93,6 +96,7 @@ constexpr uint32_t kTmemCols = 512;
 // Hardware barriers: 1 + g over Q tile g's softmax warps (merging), kBarP + g
 // over those warps and the MMA warp (P of Q tile g written)
 constexpr int kBarP = 3;
+constexpr int kBarL = kBarP + kQT;
 
 // Key tiles of row tile r of sequence q: up to the last key its last row sees.
 __host__ __device__ __forceinline__ int unit_tiles(int prefix_len, int chunk_len, int G, int r) {
@@ -466,6 +470,7 @@ __device__ __forceinline__ uint32_t prefill_cta(const PrefillParams &p, const CU
                         if (k >= 1) {
                             // O_g += P_g(k-1) V(k-1); P sits in S_g's first 64 columns
                             __syncwarp();
+                            if (g == 0) named_bar_sync(kBarL, 64);
                             named_bar_sync(kBarP + g, 160);
                             if (lane == 0) {
                                 tc_fence_after();
@@ -495,7 +500,32 @@ __device__ __forceinline__ uint32_t prefill_cta(const PrefillParams &p, const CU
                 x += nt;
             }
         }
-    } else if (warp < 2 + 4 * kQT) {  // (a wider CTA's other warps only meet the final barrier)
+    } else if (warp == 2 + 4 * kQT) {
+        // ============================================================ load watcher
+        // Tile by tile, V(j) and the segment's K(j+1) have landed before the
+        // MMA warp issues the PV of tile j and the QK of tile j+1: this warp
+        // waits on their mbarriers and then syncs with the MMA warp on a
+        // hardware barrier, so the issuing thread touches no mbarrier in the
+        // steady state
+        int gt = 0;
+        for (int x = x0; x < x1;) {
+            const Seg sg = seg_at<G>(p, x, x1);
+            const int nt = sg.t1 - sg.t0;
+            for (int k = 0; k < nt; ++k, ++gt) {
+                if (lane == 0) {
+                    const int iv = 2 * gt + 1;
+                    wait_or_flag(&full[iv % kSlots], (uint32_t)(iv / kSlots) & 1u, p.d_err);
+                    if (k + 1 < nt) {
+                        const int ik = 2 * gt + 2;
+                        wait_or_flag(&full[ik % kSlots], (uint32_t)(ik / kSlots) & 1u, p.d_err);
+                    }
+                }
+                __syncwarp();
+                named_bar_sync(kBarL, 64);
+            }
+            x += nt;
+        }
+    } else if (warp < 2 + 4 * kQT) {
         // ============================================================ softmax
         const int g = (warp - 2) >> 2;         // Q tile of this warp group
         const int quarter = warp & 3;          // TMEM lanes 32*quarter .. +31 (fixed by the warp id)
@@ -668,16 +698,6 @@ __device__ __forceinline__ uint32_t prefill_cta(const PrefillParams &p, const CU
                     }
                     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
                 }
-                if (g == 0) {
-                    // the MMAs this announcement releases read V of this tile
-                    // and K of the segment's next one
-                    const int iv = 2 * gt + 1;
-                    wait_or_flag(&full[iv % kSlots], (uint32_t)(iv / kSlots) & 1u, p.d_err);
-                    if (k + 1 < nt) {
-                        const int ik = 2 * gt + 2;
-                        wait_or_flag(&full[ik % kSlots], (uint32_t)(ik / kSlots) & 1u, p.d_err);
-                    }
-                }
                 tmem_wait_st();
                 tc_fence_before();
                 named_bar_arrive(kBarP + g, 160);
@@ -748,7 +768,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 // The prefill CTAs keep the tensor cores busy while the decode CTAs stream
 // K/V from HBM, in one grid of one CTA per SM, so neither half waits for the
 // other to release SMs.
-constexpr int kMixedThreads = kThreads + 64;  // twelve warps: two decode instances
+constexpr int kMixedThreads = kThreads + 32;  // twelve warps: two decode instances
 constexpr int kDecodeSlotsMixed = tcd::kSlotsStandalone;
 constexpr uint32_t kDecodeInst1 = (tcd::TcLayout<kDecodeSlotsMixed>::kSmemUsed + 1023u) & ~1023u;
 constexpr uint32_t kMixedHolder = kOffBar + 248;  // TMEM base of a decode-only CTA (past the prefill's barriers)
@@ -772,7 +792,7 @@ __global__ void __launch_bounds__(kMixedThreads, 1)
     if (prefill)  // ends with a CTA barrier: every warp is past the prefill's use of shared memory and TMEM
         tmem = prefill_cta<T, BS, G, true>(mp.pp, tmk, tmv, tmq, (int)blockIdx.x, mp.prefill_ctas);
     tcd::TcRun r;
-    tcd::tc_init<kDecodeSlotsMixed>(r, inst * kDecodeInst1, inst * 6, 5 + inst);
+    tcd::tc_init<kDecodeSlotsMixed>(r, inst * kDecodeInst1, inst * 6, kBarL + 1 + inst);
     if (!prefill && warp == 1) tcd::tc_alloc(holder, 2 * tcd::kTmemCols);
     tc_fence_before();
     __syncthreads();
