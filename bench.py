@@ -46,28 +46,40 @@ def load_peaks():
     return FALLBACK_HBM_GBS, "fallback"
 
 
-def load_traffic(kernel_key: str, source: str = "pa_decode.cuh"):
+def source_hash(source: str) -> str:
+    import hashlib
+    src = os.path.join(ROOT, "paged_kv_cache_224_gb300", "csrc", source)
+    return hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+
+
+def load_traffic(kernel_key: str, sources):
     """Per-launch DRAM bytes of a kernel from the committed ncu summary, if
-    it was taken on the current kernel source (an entry lists the hash of
-    every source file it depends on, comma-separated)."""
+    it was taken on the current sources: an entry lists the hash of every
+    source file the kernel is built from, comma-separated, and each of
+    `sources` must be among them."""
     path = os.path.join(ROOT, "profiles", "traffic.txt")
     if not os.path.exists(path):
         return None
-    import hashlib
-    src = os.path.join(ROOT, "paged_kv_cache_224_gb300", "csrc", source)
-    sha = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+    want = [source_hash(s) for s in sources]
     for line in open(path):
         parts = line.split()
-        if len(parts) >= 3 and parts[0] == kernel_key and sha in parts[1].split(","):
+        if len(parts) >= 3 and parts[0] == kernel_key and all(h in parts[1].split(",") for h in want):
             return float(parts[2])
     return None
 
 
+# The files each kernel is compiled from (its own source and the device
+# headers it includes), for the traffic entries' hashes.
+DECODE_SOURCES = ["pa_decode.cuh", "pa_device.cuh"]
+DECODE_TC_SOURCES = ["pa_decode_tc.cuh", "pa_decode_tc.cu", "pa_tcgen05.cuh", "pa_device.cuh"]
+PREFILL_SOURCES = ["pa_prefill.cu", "pa_decode_tc.cuh", "pa_tcgen05.cuh", "pa_device.cuh"]
+
+
 def decode_kernel_of(group: int, head_dim: int):
-    """The decode kernel the library runs for a head group, and its source file."""
+    """The decode kernel the library runs for a head group, and its sources."""
     if group == 8 and head_dim == 128:
-        return "decode_tc_kernel", "pa_decode_tc.cu"
-    return "decode_kernel", "pa_decode.cuh"
+        return "decode_tc_kernel", DECODE_TC_SOURCES
+    return "decode_kernel", DECODE_SOURCES
 
 
 class ClockSampler:
@@ -307,7 +319,7 @@ def run_prefill_bench(args, world, rank, local, dev, stream):
                            "l2": "each kv head's KV is reused from L2 by its row tiles"},
                 "roofline": {"bound": "tensor", "achieved": round(achieved, 2), "peak": peak,
                              "unit": "TFLOP/s", "frac": round(achieved / peak, 4),
-                             "traffic": load_traffic(case.name, "pa_prefill.cu"),
+                             "traffic": load_traffic(case.name, PREFILL_SOURCES),
                              "kernel": "prefill_tc_kernel", "flops_per_launch": flops, "avg_ms": round(pf_ms, 5),
                              "peak_kind": f"{kind} (bf16 dense, burst)"},
                 "gpu_launches": 2 * args.steps, "clocks": clk.summary()}
@@ -399,7 +411,7 @@ def run_mixed_bench(args, world, rank, local, dev, stream):
                 "overlap_gain": round(ms_seq / ms_mixed - 1.0, 4),
                 "prefill_tflops_in_step": round(case.prefill_flops() / (ms_mixed / 1e3) / 1e12, 2),
                 "roofline": {"bound": "hbm", "achieved": round(dec_gbs, 2), "peak": peak, "unit": "GB/s",
-                             "frac": round(dec_gbs / peak, 4), "traffic": None,
+                             "frac": round(dec_gbs / peak, 4), "traffic": load_traffic(case.name, PREFILL_SOURCES),
                              "kernel": "the decode half's KV streamed per step while the prompt chunk runs",
                              "bytes_per_launch": case.decode_bytes(), "avg_ms": round(ms_mixed, 5),
                              "peak_kind": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)"},
@@ -563,8 +575,7 @@ def main():
         # three kernels (prefix pass, tail pass, reduce): the traffic entry is
         # their sum, valid while both decode sources are unchanged
         pre_src = decode_kernel_of(G * case.group_size, case.head_dim)[1]
-        t_pre = load_traffic(f"decode_{case.name}_grouped", pre_src)
-        traffic = load_traffic(f"decode_{case.name}_grouped", ksrc) if t_pre is not None else None
+        traffic = load_traffic(f"decode_{case.name}_grouped", sorted(set(pre_src) | set(ksrc)))
     else:
         traffic = load_traffic(f"decode_{case.name}", ksrc)
 
