@@ -113,6 +113,9 @@ def test_mixed_step_equals_the_two_calls_and_the_oracle(G, dtype):
     ([1000, 5], [64, 700], [5000, 1, 17, 2048, 128, 4097], 32, "bf16"),
     ([0], [1], [3], 16, "bf16"),
     ([8192], [512], [int(x) for x in np.random.default_rng(3).integers(1, 4097, size=40)], 16, "bf16"),
+    ([130, 0, 4000], [200, 9, 64], [64, 1, 4096, 1000, 0, 63], 64, "f16"),
+    ([2048], [333], [1, 127, 128, 129, 5000, 16384], 128, "bf16"),
+    ([0, 5], [1, 1], [int(x) for x in np.random.default_rng(4).integers(0, 600, size=700)], 16, "bf16"),
 ])
 def test_mixed_step_one_launch_matches_the_oracle(prefix, chunks, lens, bs, dtype):
     # one launch (8 query heads per kv head, a mixed-step workspace): every
