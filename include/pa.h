@@ -234,8 +234,10 @@ PA_API int pa_decode_noalloc(void *out, const void *query, const void *k_cache, 
  * generated token: copy-on-write of shared blocks, the new tokens' K/V into
  * their slots, then attention; "vLLM PagedAttention chuyen sau"
  * (locionic.com), sections "Co che PagedAttention" and "Co che APC").
- * In order on `stream`: each host input is copied into `staging` (one
- * cudaMemcpyAsync per input), then pa_copy_blocks (when num_pairs > 0),
+ * In order on `stream`: the host inputs are brought into `staging` -- those
+ * in page-locked host memory the device can address by one gather kernel
+ * that reads them all, any other with its own cudaMemcpyAsync -- then
+ * pa_copy_blocks (when num_pairs > 0),
  * pa_reshape_and_cache (when num_new_tokens > 0), pa_decode -- or
  * pa_decode_shared_prefix when group_size > 1 -- into staging, and the
  * output is copied to out_host.  All of it is asynchronous: the host buffers

@@ -521,8 +521,24 @@ int pa_decode_step_host(void *out_host, const void *query_host, const void *new_
     const size_t ws_bytes = lay.total - lay.off[9];
     const size_t qbytes = (size_t)num_seqs * num_heads * head_dim * 2;
     const size_t kvbytes = (size_t)num_new_tokens * num_kv_heads * head_dim * 2;
+    // Inputs in page-locked host memory the device can address are read by
+    // one gather kernel (the copies' fixed costs, paid once); any other input
+    // is copied with its own cudaMemcpyAsync.
+    pa::GatherList gl{};
     auto h2d = [&](void *dst, const void *src, size_t n) {
-        return n == 0 || cudaMemcpyAsync(dst, src, n, cudaMemcpyHostToDevice, st) == cudaSuccess;
+        if (n == 0) return true;
+        cudaPointerAttributes at{};
+        const cudaError_t qa = cudaPointerGetAttributes(&at, src);
+        if (qa != cudaSuccess) cudaGetLastError();  // a pointer the runtime does not know: no error kept
+        if (qa == cudaSuccess && at.type == cudaMemoryTypeHost && at.devicePointer != nullptr &&
+            gl.n < pa::kGatherMax) {
+            gl.src[gl.n] = at.devicePointer;
+            gl.dst[gl.n] = dst;
+            gl.bytes[gl.n] = n;
+            ++gl.n;
+            return true;
+        }
+        return cudaMemcpyAsync(dst, src, n, cudaMemcpyHostToDevice, st) == cudaSuccess;
     };
     if (!h2d(d_q, query_host, qbytes) || !h2d(d_k, new_key_host, kvbytes) || !h2d(d_v, new_value_host, kvbytes) ||
         !h2d(d_slots, slot_mapping_host, (size_t)num_new_tokens * 8) ||
@@ -530,6 +546,7 @@ int pa_decode_step_host(void *out_host, const void *query_host, const void *new_
         !h2d(d_bt, block_tables_host, (size_t)num_seqs * max_blocks_per_seq * 4) ||
         !h2d(d_lens, context_lens_host, (size_t)num_seqs * 4))
         return PA_ERR_CUDA;
+    if (pa::launch_gather(gl, st) != PA_OK) return PA_ERR_CUDA;
     int rc = pa_copy_blocks(k_cache, v_cache, d_pairs, num_pairs, num_kv_heads, head_dim, block_size, num_blocks,
                             dtype, d_cow_ws, cow_ws_bytes, d_err, stream);
     if (rc != PA_OK) return rc;

@@ -201,4 +201,40 @@ int launch_copy_blocks(void *k_cache, void *v_cache, const int64_t *pairs, int n
     return cudaPeekAtLastError() == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }
 
+// ---- gather --------------------------------------------------------------------
+//
+// One launch for a step's small inputs: each CTA strides over the items'
+// 16-byte units (or bytes, for an item whose ends or size are not 16-byte
+// multiples) so the copies run side by side instead of one after another.
+__global__ void __launch_bounds__(256)
+gather_kernel(const __grid_constant__ GatherList list) {
+    const long long stride = (long long)gridDim.x * blockDim.x;
+    const long long t0 = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+    for (int it = 0; it < list.n; ++it) {
+        const unsigned long long nb = list.bytes[it];
+        const bool vec = ((reinterpret_cast<uintptr_t>(list.src[it]) | reinterpret_cast<uintptr_t>(list.dst[it]) |
+                           (uintptr_t)nb) & 15u) == 0;
+        if (vec) {
+            const uint4 *s = static_cast<const uint4 *>(list.src[it]);
+            uint4 *d = static_cast<uint4 *>(list.dst[it]);
+            for (long long i = t0; i < (long long)(nb / 16); i += stride) d[i] = s[i];
+        } else {
+            const unsigned char *s = static_cast<const unsigned char *>(list.src[it]);
+            unsigned char *d = static_cast<unsigned char *>(list.dst[it]);
+            for (long long i = t0; i < (long long)nb; i += stride) d[i] = s[i];
+        }
+    }
+}
+
+int launch_gather(const GatherList &list, cudaStream_t stream) {
+    if (list.n <= 0) return PA_OK;
+    if (list.n > kGatherMax) return PA_ERR_INVALID_ARG;
+    unsigned long long units = 0;
+    for (int i = 0; i < list.n; ++i) units += (list.bytes[i] + 15) / 16;
+    const long long blocks = std::min<long long>(std::max<long long>(1, (long long)((units + 255) / 256)),
+                                                 (long long)sm_count() * 4);
+    gather_kernel<<<(unsigned)blocks, 256, 0, stream>>>(list);
+    return cudaPeekAtLastError() == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+}
+
 }  // namespace pa

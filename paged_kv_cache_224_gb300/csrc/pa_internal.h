@@ -133,6 +133,18 @@ int launch_decode_reduce(pa_dtype dt, int head_dim, const DecodeParams &p, cudaS
 int launch_reshape_and_cache(const void *key, const void *value, void *k_cache, void *v_cache,
                              const int64_t *slots, int num_tokens, int num_kv_heads, int head_dim,
                              int block_size, int num_blocks, int *d_err, cudaStream_t stream);
+// Copies of up to kGatherMax buffers in one launch, each from memory the
+// device can address (pinned host memory through its device view included)
+// to device memory: 16-byte vectors where both ends and the size allow,
+// bytes otherwise.
+constexpr int kGatherMax = 8;
+struct GatherList {
+    const void *src[kGatherMax];
+    void *dst[kGatherMax];
+    unsigned long long bytes[kGatherMax];
+    int n;
+};
+int launch_gather(const GatherList &list, cudaStream_t stream);
 size_t copy_blocks_workspace_bytes(int num_pairs);
 int launch_copy_blocks(void *k_cache, void *v_cache, const int64_t *pairs, int num_pairs,
                        int num_kv_heads, int head_dim, int block_size, int num_blocks, void *workspace,

@@ -110,3 +110,38 @@ def test_host_step_without_new_tokens_or_pairs():
     torch.cuda.synchronize()
     assert torch.equal(out, ref.cpu())
     assert torch.equal(t["k_cache"], before)
+
+
+def test_host_step_pageable_and_unaligned_inputs_equal_the_pinned_step():
+    # page-locked inputs are read by one gather kernel (16-byte vectors, or
+    # bytes when an end or the size is not a multiple of 16); anything else
+    # is copied with cudaMemcpyAsync.  Both routes give the same bits.
+    c = wl.make_decode_case("host_mix", [5, 130, 701, 33, 1000], 8, 2, 128, 16, "bf16", seed=67)
+    t = c.materialize(DEV)
+    t_pin, t_page, t_odd = ({k: v.clone() for k, v in t.items()} for _ in range(3))
+    out_pin = host_step(c, t_pin, False, 0)
+
+    def run(tt, conv):
+        out = torch.full(tuple(tt["query"].shape), float("nan"), dtype=tt["query"].dtype).pin_memory()
+        err = torch.zeros(1, dtype=torch.int32, device=DEV)
+        pa.pa_decode_step_host(out, conv(tt["query"]), conv(tt["new_key"]), conv(tt["new_value"]),
+                               conv(torch.as_tensor(c.slot_mapping)), conv(torch.as_tensor(c.block_tables)),
+                               conv(torch.as_tensor(c.context_lens)), tt["k_cache"], tt["v_cache"], c.scale,
+                               c.max_context_len, d_err=err)
+        torch.cuda.synchronize()
+        assert int(err.item()) == 0
+        return out
+
+    def odd(x):
+        # page-locked, but starting one element past a 16-byte boundary
+        x = x.cpu()
+        buf = torch.empty(x.numel() + 1, dtype=x.dtype).pin_memory()
+        v = buf[1:].view(x.shape)
+        v.copy_(x)
+        return v
+
+    out_page = run(t_page, lambda x: x.cpu())
+    out_odd = run(t_odd, odd)
+    assert torch.equal(out_page, out_pin) and torch.equal(out_odd, out_pin)
+    for tt in (t_page, t_odd):
+        assert torch.equal(tt["k_cache"], t_pin["k_cache"]) and torch.equal(tt["v_cache"], t_pin["v_cache"])
