@@ -233,3 +233,35 @@ def test_mixed_step_with_one_half_empty_runs_that_half_alone():
     torch.cuda.synchronize()
     assert int(err.item()) == 0
     assert torch.equal(dout, ds) and torch.equal(pout, ps)
+
+
+def _random_mixed_configs(n, seed):
+    rng = np.random.default_rng(seed)
+    out = []
+    for i in range(n):
+        nd = int(rng.choice([1, 3, 17, 90]))
+        lens = [int(x) for x in rng.integers(0, int(rng.choice([64, 1500, 5000])), size=nd)]
+        npf = int(rng.integers(1, 4))
+        prefix = [int(x) for x in rng.integers(0, 2000, size=npf)]
+        chunks = [int(x) for x in rng.integers(0, 400, size=npf)]
+        chunks[0] = max(chunks[0], 1)
+        hkv = int(rng.integers(1, 4))
+        bs = int(rng.choice([16, 32, 64, 128]))
+        dtype = str(rng.choice(["f16", "bf16"]))
+        out.append((i, lens, prefix, chunks, hkv, bs, dtype))
+    return out
+
+
+@pytest.mark.parametrize("i,lens,prefix,chunks,hkv,bs,dtype", _random_mixed_configs(10, 4242))
+def test_mixed_step_one_launch_random_shapes(i, lens, prefix, chunks, hkv, bs, dtype):
+    # 8 query heads per kv head (the one-launch kernel's shape), everything
+    # else drawn: every output of both halves against the oracle
+    c = wl.make_mixed_case(f"mixrand{i}", lens, prefix, chunks, 8 * hkv, hkv, 128, bs, dtype, seed=500 + i)
+    t = c.materialize(DEV)
+    err = torch.zeros(1, dtype=torch.int32, device=DEV)
+    write_step_kv(c, t, err)
+    ws = pa.mixed_workspace(t["prefill_query"], t["decode_query"], hkv, bs, len(chunks), c.max_context_len)
+    pm, dm = mixed(c, t, err, workspace=ws)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0, f"device error flags {int(err.item()):#x}"
+    check_both_halves(c, t, pm, dm, f"random mixed {i}")
