@@ -1,7 +1,10 @@
 // Device code of the tensor-core decode (head groups up to 8 at head_dim 128),
 // shared by the decode kernel (one unit per CTA, two CTAs per SM) and the
-// mixed prefill + decode kernel (a persistent decode role, one CTA per SM with
-// a deeper ring).  See pa_decode_tc.cu for the design.
+// one-launch mixed prefill + decode kernel (two six-warp decode instances per
+// CTA, each drawing units from a queue the grid shares).  An instance is a
+// producer warp, an MMA warp and four softmax warps with their own three-slot
+// ring, barriers and 64 TMEM columns; its ring, barrier phases and TMEM run on
+// from one unit to the next.  See pa_decode_tc.cu for the design.
 #pragma once
 
 #include <cuda.h>
