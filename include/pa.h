@@ -239,8 +239,10 @@ PA_API int pa_decode_noalloc(void *out, const void *query, const void *k_cache, 
  * that reads them all, any other with its own cudaMemcpyAsync -- then
  * pa_copy_blocks (when num_pairs > 0),
  * pa_reshape_and_cache (when num_new_tokens > 0), pa_decode -- or
- * pa_decode_shared_prefix when group_size > 1 -- into staging, and the
- * output is copied to out_host.  All of it is asynchronous: the host buffers
+ * pa_decode_shared_prefix when group_size > 1 -- and the output lands in
+ * out_host: written there by the kernels when out_host is page-locked host
+ * memory the device can address (16-byte aligned), else written into staging
+ * and copied with cudaMemcpyAsync.  All of it is asynchronous: the host buffers
  * must stay valid and unchanged until the stream has finished the step, and
  * out_host holds the result only after the caller synchronises.  Host
  * buffers should be page-locked (pinned) for the copies to be asynchronous.

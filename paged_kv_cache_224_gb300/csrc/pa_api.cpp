@@ -511,6 +511,19 @@ int pa_decode_step_host(void *out_host, const void *query_host, const void *new_
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     char *base = static_cast<char *>(staging);
     void *d_out = base + lay.off[0], *d_q = base + lay.off[1], *d_k = base + lay.off[2], *d_v = base + lay.off[3];
+    // An output in page-locked host memory the device can address is written
+    // there by the kernels themselves (no copy after the step).
+    bool out_direct = false;
+    {
+        cudaPointerAttributes at{};
+        const cudaError_t qa = cudaPointerGetAttributes(&at, out_host);
+        if (qa != cudaSuccess) cudaGetLastError();
+        if (qa == cudaSuccess && at.type == cudaMemoryTypeHost && at.devicePointer != nullptr &&
+            aligned16(at.devicePointer)) {
+            d_out = at.devicePointer;
+            out_direct = true;
+        }
+    }
     int64_t *d_slots = reinterpret_cast<int64_t *>(base + lay.off[4]);
     int64_t *d_pairs = reinterpret_cast<int64_t *>(base + lay.off[5]);
     int32_t *d_bt = reinterpret_cast<int32_t *>(base + lay.off[6]);
@@ -563,6 +576,7 @@ int pa_decode_step_host(void *out_host, const void *query_host, const void *new_
                        num_kv_heads, head_dim, block_size, num_blocks, max_context_len, scale, partition_tokens,
                        dtype, d_ws, ws_bytes, d_err, stream);
     if (rc != PA_OK) return rc;
+    if (out_direct) return PA_OK;
     return cudaMemcpyAsync(out_host, d_out, qbytes, cudaMemcpyDeviceToHost, st) == cudaSuccess ? PA_OK
                                                                                                   : PA_ERR_CUDA;
 }

@@ -114,15 +114,16 @@ def test_host_step_without_new_tokens_or_pairs():
 
 def test_host_step_pageable_and_unaligned_inputs_equal_the_pinned_step():
     # page-locked inputs are read by one gather kernel (16-byte vectors, or
-    # bytes when an end or the size is not a multiple of 16); anything else
-    # is copied with cudaMemcpyAsync.  Both routes give the same bits.
+    # bytes when an end or the size is not a multiple of 16) and a
+    # page-locked, aligned output is written by the kernels in place; anything
+    # else is copied with cudaMemcpyAsync.  Every route gives the same bits.
     c = wl.make_decode_case("host_mix", [5, 130, 701, 33, 1000], 8, 2, 128, 16, "bf16", seed=67)
     t = c.materialize(DEV)
     t_pin, t_page, t_odd = ({k: v.clone() for k, v in t.items()} for _ in range(3))
     out_pin = host_step(c, t_pin, False, 0)
 
     def run(tt, conv):
-        out = torch.full(tuple(tt["query"].shape), float("nan"), dtype=tt["query"].dtype).pin_memory()
+        out = conv(torch.full(tuple(tt["query"].shape), float("nan"), dtype=tt["query"].dtype))
         err = torch.zeros(1, dtype=torch.int32, device=DEV)
         pa.pa_decode_step_host(out, conv(tt["query"]), conv(tt["new_key"]), conv(tt["new_value"]),
                                conv(torch.as_tensor(c.slot_mapping)), conv(torch.as_tensor(c.block_tables)),
