@@ -265,3 +265,34 @@ def test_mixed_step_one_launch_random_shapes(i, lens, prefix, chunks, hkv, bs, d
     torch.cuda.synchronize()
     assert int(err.item()) == 0, f"device error flags {int(err.item()):#x}"
     check_both_halves(c, t, pm, dm, f"random mixed {i}")
+
+
+def test_mixed_step_one_launch_flags_a_bad_table_entry_and_finishes():
+    # one decode sequence's table names a block past the pool: the kernel
+    # fetches zeros for it, leaves it out of that sequence's softmax, flags
+    # block_range and completes; the prompt chunk and the other decodes are
+    # unaffected
+    c = wl.make_mixed_case("mixbad", [700, 300, 50], [200], [64], 16, 2, 128, 16, "bf16", seed=77)
+    t = c.materialize(DEV)
+    err = torch.zeros(1, dtype=torch.int32, device=DEV)
+    write_step_kv(c, t, err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    pbt, dbt, lens = device_args(c)
+    dbt[0, 3] = c.num_blocks + 1000
+    ws = pa.mixed_workspace(t["prefill_query"], t["decode_query"], 2, 16, 1, c.max_context_len)
+    pout = torch.full_like(t["prefill_query"], float("nan"))
+    dout = torch.full_like(t["decode_query"], float("nan"))
+    pa.pa_mixed_step(pout, t["prefill_query"], pbt, c.prefix_lens, c.chunk_lens, dout, t["decode_query"], dbt,
+                     lens, t["k_cache"], t["v_cache"], c.scale, c.max_context_len, workspace=ws, d_err=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) & pa.capi.DEVERR["block_range"]
+    assert not int(err.item()) & pa.capi.DEVERR["timeout"]
+    kc, vc = wl.bits(t["k_cache"]), wl.bits(t["v_cache"])
+    ref_d = oracle.decode(wl.bits(t["decode_query"]), kc, vc, c.decode_tables, c.context_lens, c.scale, c.dtype,
+                          num_threads=8)
+    check_attention(to_f64(dout[1:]), ref_d[1:], c.dtype, "decodes with good tables")
+    assert np.isfinite(to_f64(dout[0])).all()
+    ref_p = oracle.prefill_chunk(wl.bits(t["prefill_query"]), kc, vc, c.prefill_tables[0], int(c.prefix_lens[0]),
+                                 c.scale, c.dtype, num_threads=8)
+    check_attention(to_f64(pout), ref_p, c.dtype, "prompt chunk")
