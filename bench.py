@@ -72,7 +72,9 @@ def load_traffic(kernel_key: str, sources):
 # headers it includes), for the traffic entries' hashes.
 DECODE_SOURCES = ["pa_decode.cuh", "pa_device.cuh"]
 DECODE_TC_SOURCES = ["pa_decode_tc.cuh", "pa_decode_tc.cu", "pa_tcgen05.cuh", "pa_device.cuh"]
-PREFILL_SOURCES = ["pa_prefill.cu", "pa_decode_tc.cuh", "pa_tcgen05.cuh", "pa_device.cuh"]
+PREFILL_SOURCES = ["pa_prefill.cu", "pa_prefill.cuh", "pa_tcgen05.cuh", "pa_device.cuh"]
+MIXED_SOURCES = ["pa_mixed.cuh", "pa_mixed_bf16.cu", "pa_prefill.cuh", "pa_decode_tc.cuh", "pa_tcgen05.cuh",
+                 "pa_device.cuh"]
 
 
 def decode_kernel_of(group: int, head_dim: int):
@@ -411,7 +413,7 @@ def run_mixed_bench(args, world, rank, local, dev, stream):
                 "overlap_gain": round(ms_seq / ms_mixed - 1.0, 4),
                 "prefill_tflops_in_step": round(case.prefill_flops() / (ms_mixed / 1e3) / 1e12, 2),
                 "roofline": {"bound": "hbm", "achieved": round(dec_gbs, 2), "peak": peak, "unit": "GB/s",
-                             "frac": round(dec_gbs / peak, 4), "traffic": load_traffic(case.name, PREFILL_SOURCES),
+                             "frac": round(dec_gbs / peak, 4), "traffic": load_traffic(case.name, MIXED_SOURCES),
                              "kernel": "the decode half's KV streamed per step while the prompt chunk runs",
                              "bytes_per_launch": case.decode_bytes(), "avg_ms": round(ms_mixed, 5),
                              "peak_kind": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)"},

@@ -287,7 +287,7 @@ PA_API int pa_decode_step_host(void *out_host, const void *query_host, const voi
  * the host) and pa_decode (decode_*, context_lens on the device), with the
  * pool and the model shape shared.
  *
- * One launch: with head_dim 128, 8 query heads per kv head, block_size 16 to
+ * One launch: with head_dim 128, 2, 4 or 8 query heads per kv head, block_size 16 to
  * 128, max_context_len <= 16384, at most 64 non-empty chunks, and a
  * workspace of at least pa_mixed_step_workspace_bytes(...) bytes, 256-byte
  * aligned and ZERO-FILLED before its first use, the step is one kernel of one

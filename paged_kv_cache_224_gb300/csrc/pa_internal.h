@@ -158,6 +158,9 @@ int launch_prefill(pa_dtype dt, int head_dim, int block_size, int group, const P
 // Whether launch_mixed has a kernel for these (head_dim 128, a tensor-core
 // decode group, block_size 16..128).
 bool mixed_supported(int head_dim, int block_size, int group);
+// The one-launch step's kernel instances, one translation unit per dtype.
+int launch_mixed_bf16(int block_size, int group, const MixedParams &mp, unsigned grid, cudaStream_t stream);
+int launch_mixed_f16(int block_size, int group, const MixedParams &mp, unsigned grid, cudaStream_t stream);
 // The fused step: pp as for launch_prefill (at most kPrefillMaxSeqs chunks),
 // dp as for launch_decode with one partition per sequence; prefill_ws as for
 // launch_prefill (required); decode_bytes: the decodes' K/V bytes, estimated,

@@ -134,6 +134,26 @@ def test_mixed_step_one_launch_matches_the_oracle(prefix, chunks, lens, bs, dtyp
     check_both_halves(c, t, pm, dm, "one launch")
 
 
+@pytest.mark.parametrize("G,dtype", [(4, "bf16"), (2, "f16"), (1, "bf16")])
+def test_mixed_step_one_launch_smaller_head_groups(G, dtype):
+    # 2 or 4 query heads per kv head in one launch (the decode instances leave
+    # the rest of the MMA's 16 head rows zero; LLaMA-like 32/8 heads at
+    # G = 4); 1 runs as two launches (the CUDA-core decode)
+    hkv = 8 if G == 4 else 2
+    lens = [int(x) for x in np.random.default_rng(G).integers(1, 3000, size=60)] + [0, 1, 16384]
+    c = wl.make_mixed_case(f"mixg{G}", lens, [1500, 0], [300, 77], G * hkv, hkv, 128, 16, dtype, seed=610 + G)
+    t = c.materialize(DEV, pool_fill=float("nan"))
+    err = torch.zeros(1, dtype=torch.int32, device=DEV)
+    write_step_kv(c, t, err)
+    ws = pa.mixed_workspace(t["prefill_query"], t["decode_query"], hkv, 16, 2, c.max_context_len)
+    pm, dm = mixed(c, t, err, workspace=ws)
+    pm2, dm2 = mixed(c, t, err, workspace=ws)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0, f"device error flags {int(err.item()):#x}"
+    assert torch.equal(pm, pm2) and torch.equal(dm, dm2)
+    check_both_halves(c, t, pm, dm, f"one launch, G={G}")
+
+
 def test_mixed_step_one_launch_workspace_shared_by_steps_of_other_shapes():
     # the decode queue's counter and the stream-K counters live in the
     # workspace and must be back at zero after every step, whatever its shape:
@@ -248,15 +268,16 @@ def _random_mixed_configs(n, seed):
         hkv = int(rng.integers(1, 4))
         bs = int(rng.choice([16, 32, 64, 128]))
         dtype = str(rng.choice(["f16", "bf16"]))
-        out.append((i, lens, prefix, chunks, hkv, bs, dtype))
+        G = int(rng.choice([1, 2, 4, 8]))
+        out.append((i, lens, prefix, chunks, G, hkv, bs, dtype))
     return out
 
 
-@pytest.mark.parametrize("i,lens,prefix,chunks,hkv,bs,dtype", _random_mixed_configs(10, 4242))
-def test_mixed_step_one_launch_random_shapes(i, lens, prefix, chunks, hkv, bs, dtype):
-    # 8 query heads per kv head (the one-launch kernel's shape), everything
-    # else drawn: every output of both halves against the oracle
-    c = wl.make_mixed_case(f"mixrand{i}", lens, prefix, chunks, 8 * hkv, hkv, 128, bs, dtype, seed=500 + i)
+@pytest.mark.parametrize("i,lens,prefix,chunks,G,hkv,bs,dtype", _random_mixed_configs(12, 4242))
+def test_mixed_step_one_launch_random_shapes(i, lens, prefix, chunks, G, hkv, bs, dtype):
+    # everything drawn (head groups 2-8 run in one launch, 1 in two): every
+    # output of both halves against the oracle
+    c = wl.make_mixed_case(f"mixrand{i}", lens, prefix, chunks, G * hkv, hkv, 128, bs, dtype, seed=500 + i)
     t = c.materialize(DEV)
     err = torch.zeros(1, dtype=torch.int32, device=DEV)
     write_step_kv(c, t, err)
